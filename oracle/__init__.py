@@ -1,0 +1,200 @@
+"""fp64 CPU oracle for exact attention -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. It computes the plain definition of
+attention (materialised score rows, two-pass safe softmax, textbook softmax
+Jacobian for the backward) in double precision; see ``oracle.c`` for the
+formulas and the passages of the pages they follow. It shares no code with
+the CUDA library.
+
+All functions take torch tensors or numpy arrays of any float dtype in the
+[B, H, N, d] layout (bias: [B, Nk]) and return float64 numpy arrays. The
+widening to float64 is exact for bf16 and fp32 inputs.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        lp = ctypes.POINTER(ctypes.c_long)
+        ip = ctypes.POINTER(ctypes.c_int)
+        ci, cd, cl = ctypes.c_int, ctypes.c_double, ctypes.c_long
+        lib.oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, cd, ci]
+        lib.oracle_fwd_rows.argtypes = [dp, dp, dp, dp, lp, ip, cl, dp, dp,
+                                        ci, ci, ci, ci, ci, cd, ci]
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp,
+                                   ci, ci, ci, ci, ci, cd, ci]
+        lib.oracle_bwd_dq_rows.argtypes = [dp, dp, dp, dp, dp, lp, ip, cl, dp,
+                                           ci, ci, ci, ci, ci, cd, ci]
+        for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_bwd,
+                  lib.oracle_bwd_dq_rows):
+            f.restype = ctypes.c_int
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(x):
+    """Exact widening of a torch tensor / array to a contiguous float64 array."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().to("cpu")
+        import torch
+        x = x.to(torch.float64).numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _shape4(q, k):
+    B, H, Nq, d = q.shape
+    Bk, Hk, Nk, dk = k.shape
+    if (Bk, Hk, dk) != (B, H, d):
+        raise ValueError("q and k/v must agree in B, H and d")
+    return B, H, Nq, Nk, d
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def fwd(q, k, v, bias=None, scale=None, causal=False):
+    """O [B,H,Nq,d] and LSE [B,H,Nq] (natural log) of the full problem."""
+    lib = _load()
+    q, k, v, bias = _f64(q), _f64(k), _f64(v), _f64(bias)
+    B, H, Nq, Nk, d = _shape4(q, k)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.empty((B, H, Nq, d))
+    lse = np.empty((B, H, Nq))
+    rc = lib.oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o), _ptr(lse),
+                        B, H, Nq, Nk, d, float(scale), int(bool(causal)))
+    if rc:
+        raise MemoryError("oracle_fwd: scratch allocation failed")
+    return o, lse
+
+
+def _head_groups(heads, rows):
+    heads = np.asarray(heads, dtype=np.int64).reshape(-1)
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1)
+    if heads.shape != rows.shape:
+        raise ValueError("heads and rows must have the same length")
+    for h in np.unique(heads):
+        idx = np.nonzero(heads == h)[0]
+        yield int(h), idx, rows[idx]
+
+
+def _head_slice(x, bh, H):
+    """[N, d] float64 slice of head bh of a [B,H,N,d] tensor (converts one head only)."""
+    b, h = divmod(bh, H)
+    return _f64(x[b, h][None, None])
+
+
+def fwd_rows(q, k, v, bias, heads, rows, scale=None, causal=False):
+    """O [n,d] and LSE [n] for the (flat head b*H+h, query row) pairs given.
+
+    Only the heads that are asked for are widened to float64, so this works
+    at full problem sizes.
+    """
+    lib = _load()
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    heads_a = np.asarray(heads, dtype=np.int64).reshape(-1)
+    o = np.empty((heads_a.size, d))
+    lse = np.empty(heads_a.size)
+    for bh, idx, r in _head_groups(heads, rows):
+        qh, kh, vh = (_head_slice(t, bh, H) for t in (q, k, v))
+        bh_bias = None if bias is None else _f64(bias[bh // H][None])
+        n = idx.size
+        hz = np.zeros(n, dtype=np.int64)                       # one head in the slice
+        rr = np.ascontiguousarray(r, dtype=np.int32)
+        oo = np.empty((n, d))
+        ll = np.empty(n)
+        rc = lib.oracle_fwd_rows(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(bh_bias),
+                                 hz.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
+                                 rr.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n,
+                                 _ptr(oo), _ptr(ll), 1, 1, Nq, Nk, d,
+                                 float(scale), int(bool(causal)))
+        if rc:
+            raise MemoryError("oracle_fwd_rows: scratch allocation failed")
+        o[idx] = oo
+        lse[idx] = ll
+    return o, lse
+
+
+def bwd(q, k, v, bias, dO, scale=None, causal=False):
+    """dQ, dK, dV [B,H,N,d] of the full problem (loss gradient dO)."""
+    lib = _load()
+    q, k, v, bias, dO = _f64(q), _f64(k), _f64(v), _f64(bias), _f64(dO)
+    B, H, Nq, Nk, d = _shape4(q, k)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.empty((B, H, Nq, d))
+    dk = np.empty((B, H, Nk, d))
+    dv = np.empty((B, H, Nk, d))
+    rc = lib.oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(dO),
+                        _ptr(dq), _ptr(dk), _ptr(dv), B, H, Nq, Nk, d,
+                        float(scale), int(bool(causal)))
+    if rc:
+        raise MemoryError("oracle_bwd: scratch allocation failed")
+    return dq, dk, dv
+
+
+def bwd_heads(q, k, v, bias, dO, heads, scale=None, causal=False):
+    """dQ, dK, dV of whole heads (flat indices), each [n_heads, N, d]."""
+    B, H, Nq, d = q.shape
+    out = []
+    for bh in heads:
+        b = bh // H
+        sl = [_head_slice(t, bh, H) for t in (q, k, v)]
+        bb = None if bias is None else _f64(bias[b][None])
+        dq, dk, dv = bwd(sl[0], sl[1], sl[2], bb, _head_slice(dO, bh, H),
+                         scale=scale, causal=causal)
+        out.append((dq[0, 0], dk[0, 0], dv[0, 0]))
+    return (np.stack([o[0] for o in out]), np.stack([o[1] for o in out]),
+            np.stack([o[2] for o in out]))
+
+
+def bwd_dq_rows(q, k, v, bias, dO, heads, rows, scale=None, causal=False):
+    """dQ [n,d] for the (flat head, query row) pairs given."""
+    lib = _load()
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    heads_a = np.asarray(heads, dtype=np.int64).reshape(-1)
+    dq = np.empty((heads_a.size, d))
+    for bh, idx, r in _head_groups(heads, rows):
+        qh, kh, vh, doh = (_head_slice(t, bh, H) for t in (q, k, v, dO))
+        bh_bias = None if bias is None else _f64(bias[bh // H][None])
+        n = idx.size
+        hz = np.zeros(n, dtype=np.int64)
+        rr = np.ascontiguousarray(r, dtype=np.int32)
+        out = np.empty((n, d))
+        rc = lib.oracle_bwd_dq_rows(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(bh_bias), _ptr(doh),
+                                    hz.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
+                                    rr.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n,
+                                    _ptr(out), 1, 1, Nq, Nk, d, float(scale),
+                                    int(bool(causal)))
+        if rc:
+            raise MemoryError("oracle_bwd_dq_rows: scratch allocation failed")
+        dq[idx] = out
+    return dq

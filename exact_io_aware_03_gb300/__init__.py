@@ -1,0 +1,169 @@
+"""Python binding of the GB300 exact-attention C ABI (include/fa.h).
+
+The functions ``fa_fwd``, ``fa_bwd``, ``fa_bwd_workspace_size``,
+``fa_status_string`` and ``fa_get_last_device_error`` have the C names and
+arguments (integers for pointers and the stream). ``fwd`` and ``bwd`` are thin
+conveniences over them for torch CUDA tensors: they only allocate the output
+tensors with torch and marshal pointers; every step of the computation runs
+in the library's CUDA kernels. There is no CPU or PyTorch fallback: if the
+library is not built, every call raises.
+"""
+import ctypes
+import os
+
+from . import build as _build
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE = range(5)
+FA_DTYPE_BF16, FA_DTYPE_FP32 = 0, 1
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status, where=""):
+        self.status = status
+        msg = fa_status_string(status) if _lib is not None else "status %d" % status
+        super().__init__("%s%s" % (where + ": " if where else "", msg))
+
+
+def library_path():
+    return _build.LIB
+
+
+def load(path=None):
+    """Load libfa_gb300.so (built by ``build.build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise ImportError("libfa_gb300.so not found at %s: run "
+                          "exact_io_aware_03_gb300.build.build() first" % path)
+    lib = ctypes.CDLL(path)
+    vp, cint, cf, csz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint, cf, cint,
+                           cint, vp]
+    lib.fa_fwd.restype = cint
+    lib.fa_bwd_workspace_size.argtypes = [cint] * 5
+    lib.fa_bwd_workspace_size.restype = csz
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint,
+                           cf, cint, cint, vp, csz, vp]
+    lib.fa_bwd.restype = cint
+    lib.fa_status_string.argtypes = [cint]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_get_last_device_error.argtypes = [vp]
+    lib.fa_get_last_device_error.restype = cint
+    _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------------ C names
+
+def fa_fwd(q, k, v, key_bias, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, stream):
+    return load().fa_fwd(q, k, v, key_bias, o, lse, B, H, Nq, Nk, d, scale, causal, dtype,
+                         stream)
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale, causal, dtype,
+           workspace, workspace_bytes, stream):
+    return load().fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale,
+                         causal, dtype, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_workspace_size(B, H, Nq, Nk, d):
+    return load().fa_bwd_workspace_size(B, H, Nq, Nk, d)
+
+
+def fa_status_string(status):
+    return load().fa_status_string(status).decode()
+
+
+def fa_get_last_device_error(stream):
+    return load().fa_get_last_device_error(stream)
+
+
+# ------------------------------------------------------------------ torch conveniences
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return FA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return FA_DTYPE_FP32
+    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _check(t, name):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous [B, H, N, d]" % name)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(t):
+    import torch
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def fwd(q, k, v, key_bias=None, causal=False, scale=None, out=None, lse=None):
+    """O [B,H,Nq,d] (q's dtype) and LSE [B,H,Nq] (fp32) for CUDA tensors [B,H,N,d]."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    if key_bias is not None:
+        _check(key_bias, "key_bias")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        st = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(key_bias), _ptr(out), _ptr(lse),
+                    B, H, Nq, Nk, d, float(scale), int(bool(causal)), _dtype_code(q),
+                    _stream(q))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+    return out, lse
+
+
+def bwd(q, k, v, o, lse, dO, key_bias=None, causal=False, scale=None, workspace=None,
+        dq=None, dk=None, dv=None):
+    """dQ, dK, dV (q's dtype) for CUDA tensors; o and lse from ``fwd`` on the same inputs."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (dO, "dO")):
+        _check(t, n)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = fa_bwd_workspace_size(B, H, Nq, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                    _ptr(dk), _ptr(dv), _ptr(key_bias), B, H, Nq, Nk, d, float(scale),
+                    int(bool(causal)), _dtype_code(q), _ptr(workspace), workspace.numel(),
+                    _stream(q))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def check_device_error(device=None):
+    """Synchronise the current stream and raise if a kernel reported a device-side timeout."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        st = fa_get_last_device_error(torch.cuda.current_stream(dev).cuda_stream)
+    if st != FA_OK:
+        raise FaError(st, "device")

@@ -1,0 +1,197 @@
+// C ABI of the library (declared in include/fa.h): argument validation,
+// TMA tensor-map encoding and dispatch to the kernels. Allocates no device
+// memory: the only device state is a per-device error word (a __device__
+// variable) whose address is looked up once per device.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+__device__ uint32_t g_fa_err_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_err_ptr[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+fa_status get_encode(EncodeTiledFn* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return FA_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = g_encode;
+  return FA_OK;
+}
+
+fa_status get_err_ptr(uint32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_err_word) != cudaSuccess || !p) return FA_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shared size/shape checks. Returns FA_OK or the error.
+fa_status check_problem(int B, int H, int Nq, int Nk, int d, float scale, fa_dtype dtype) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  if (BH >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+  if ((long long)Nq * d >= (1LL << 31) || (long long)Nk * d >= (1LL << 31))
+    return FA_ERR_INVALID_ARG;
+  // one CTA per (query-tile pair, head) must fit a 1-D grid
+  if (BH * ((Nq + 255) / 256) >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// 3-D view (d, N, B*H) of a bf16 [B][H][N][d] tensor, box (64, 128, 1),
+// 128-byte swizzle, zero fill outside the tensor.
+fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  EncodeTiledFn enc = nullptr;
+  fa_status st = get_encode(&enc);
+  if (st != FA_OK) return st;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dim or dtype";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+    case FA_ERR_DEVICE: return "FA_ERR_DEVICE: a kernel timed out on a device-side wait";
+  }
+  return "unknown fa_status";
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, const float* key_bias, void* o,
+                 float* lse, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                 fa_dtype dtype, void* stream) {
+  fa_status st = check_problem(B, H, Nq, Nk, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return FA_ERR_INVALID_ARG;
+  if ((key_bias && !aligned(key_bias, 4)) || (lse && !aligned(lse, 4))) return FA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fa::Problem p{B, H, Nq, Nk, d, scale, causal ? 1 : 0};
+
+  if (dtype == FA_DTYPE_FP32) {
+    fa::FwdF32Args a{p, static_cast<const float*>(q), static_cast<const float*>(k),
+                     static_cast<const float*>(v), key_bias, static_cast<float*>(o), lse};
+    return fa::launch_fwd_f32(a, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+  if (!lse) return FA_ERR_INVALID_ARG;
+  fa::FwdBf16Args a;
+  std::memset(&a, 0, sizeof(a));
+  a.p = p;
+  const int BH = B * H;
+  if ((st = make_map(&a.tm_q, q, BH, Nq, d)) != FA_OK) return st;
+  if ((st = make_map(&a.tm_k, k, BH, Nk, d)) != FA_OK) return st;
+  if ((st = make_map(&a.tm_v, v, BH, Nk, d)) != FA_OK) return st;
+  a.bias = key_bias;
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
+  if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
+  return fa::launch_fwd_bf16(a, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
+  const size_t rows = (size_t)B * H * Nq;
+  return round256(rows * 4) + round256(rows * (size_t)d * 4);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv, const float* key_bias, int B,
+                 int H, int Nq, int Nk, int d, float scale, int causal, fa_dtype dtype,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status st = check_problem(B, H, Nq, Nk, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
+  for (const void* ptr : p16)
+    if (!aligned(ptr, 16)) return FA_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || (key_bias && !aligned(key_bias, 4)) || !aligned(workspace, 256))
+    return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < fa_bwd_workspace_size(B, H, Nq, Nk, d)) return FA_ERR_INVALID_ARG;
+
+  fa::BwdBf16Args a;
+  std::memset(&a, 0, sizeof(a));
+  a.p = fa::Problem{B, H, Nq, Nk, d, scale, causal ? 1 : 0};
+  const int BH = B * H;
+  if ((st = make_map(&a.tm_q, q, BH, Nq, d)) != FA_OK) return st;
+  if ((st = make_map(&a.tm_k, k, BH, Nk, d)) != FA_OK) return st;
+  if ((st = make_map(&a.tm_v, v, BH, Nk, d)) != FA_OK) return st;
+  if ((st = make_map(&a.tm_do, dO, BH, Nq, d)) != FA_OK) return st;
+  a.o = static_cast<const uint16_t*>(o);
+  a.dO = static_cast<const uint16_t*>(dO);
+  a.lse = lse;
+  a.bias = key_bias;
+  const size_t rows = (size_t)BH * Nq;
+  a.D = static_cast<float*>(workspace);
+  a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * 4));
+  a.dq = static_cast<uint16_t*>(dq);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
+  if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
+  cudaError_t e = fa::launch_bwd_bf16(a, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_get_last_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  uint32_t w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_fa_err_word, sizeof(w)) != cudaSuccess) return FA_ERR_CUDA;
+  if (w) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_fa_err_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_DEVICE;
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Internal launch interface between the C ABI (fa_api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Problem description shared by all kernels. Tensors are [B][H][N][d].
+struct Problem {
+  int B, H, Nq, Nk, d;
+  float scale;   // multiplies Q K^T
+  int causal;    // bottom-right causal mask when non-zero
+};
+
+struct FwdF32Args {
+  Problem p;
+  const float* q;
+  const float* k;
+  const float* v;
+  const float* bias;   // [B][Nk] or nullptr
+  float* o;
+  float* lse;          // may be nullptr
+};
+
+// bf16 tensor-core forward. Tensor maps view each tensor as 3-D
+// (d, N, B*H) with a (64, 128, 1) box and 128-byte swizzle.
+struct FwdBf16Args {
+  Problem p;
+  CUtensorMap tm_q, tm_k, tm_v;
+  const float* bias;   // [B][Nk] or nullptr
+  uint16_t* o;         // bf16 [B][H][Nq][d]
+  float* lse;
+  uint32_t* err;       // device error word
+};
+
+struct BwdBf16Args {
+  Problem p;
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  const uint16_t* o;
+  const uint16_t* dO;
+  const float* lse;
+  const float* bias;
+  float* D;            // workspace: rowsum(dO o O), [B][H][Nq]
+  float* dq_acc;       // workspace: fp32 dQ accumulator [B][H][Nq][d]
+  uint16_t* dq;
+  uint16_t* dk;
+  uint16_t* dv;
+  uint32_t* err;
+};
+
+cudaError_t launch_fwd_f32(const FwdF32Args& a, cudaStream_t s);
+cudaError_t launch_fwd_bf16(const FwdBf16Args& a, cudaStream_t s);
+cudaError_t launch_bwd_bf16(const BwdBf16Args& a, cudaStream_t s);
+
+}  // namespace fa

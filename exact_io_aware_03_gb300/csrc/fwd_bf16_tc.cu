@@ -1,0 +1,491 @@
+// bf16 forward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Dataflow (query-tile outer, key/value tiles streamed: the order of
+// "FlashAttention, Explained", §20, with the online-softmax merge of
+// "Understanding FlashAttention Pt 1", §2.4):
+//
+//   one CTA = two 128-row query tiles Q0, Q1 of one (b, h), kept in shared
+//   memory; K_j / V_j tiles of 128 keys stream through an NS-stage ring.
+//   For each key tile j and each query tile t:
+//     S_t   = Q_t K_j^T              tcgen05.mma, fp32 accumulator in TMEM
+//     P_t   = exp2(S_t*c - m_t)      softmax warps: TMEM -> registers -> TMEM
+//                                    (P overwrites S in place as packed bf16)
+//     O_t  += P_t V_j                tcgen05.mma with A read from TMEM
+//   and after the last tile O = O_t / l_t, LSE = ln 2 * (m_t + log2 l_t).
+//
+// Warp roles (320 threads, one CTA per SM):
+//   warps 0-3   softmax for Q0 (thread = query row = TMEM lane)
+//   warps 4-7   softmax for Q1
+//   warp  8     TMA producer (one lane)
+//   warp  9     TMEM allocator + MMA issuer (one lane)
+// The MMA order S0(j) S1(j) | PV0(j) S0(j+1) | PV1(j) S1(j+1) | ... lets the
+// tensor core work on one query tile while the softmax warps of the other
+// tile exponentiate (two tiles in ping-pong).
+//
+// TMEM (512 columns): S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D),
+// O1 [256+D, 256+2D).
+//
+// Softmax details:
+//  - exponentials in base 2 with scale*log2(e) folded in ("flash-attention",
+//    Part VI);
+//  - the running max is only moved when the new tile's max exceeds it by more
+//    than kRescaleLog2 (8, i.e. a factor 256): otherwise P is formed against the
+//    stale max, which keeps every p <= 2^8 and the result exact, and saves the
+//    rescale of O in TMEM. The rescale of O, when needed, is done by the
+//    softmax warps themselves after the previous PV product has completed;
+//  - causal tiles wholly above the bottom-right diagonal are skipped, only
+//    tiles that cross it (or the ragged last key tile) are masked element by
+//    element ("Understanding FlashAttention Pt 1", §3.5);
+//  - key tiles outside the first/last key with a finite bias are skipped
+//    (they contribute exactly zero);
+//  - a row with no visible key keeps m = -inf and l = 0 and is written as
+//    O = 0, LSE = -inf.
+#include <cmath>
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kBM = 128;       // rows per query tile (= TMEM lanes)
+constexpr int kBN = 128;       // keys per key tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NS = (D == 128) ? 2 : 4;            // K/V ring stages
+  static constexpr int TILE = kBM * D * 2;                 // bytes of one bf16 tile
+  static constexpr int SUB = kBM * 128;                    // bytes of one 64-column box
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = 2 * TILE;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_MISC = OFF_V + NS * TILE;
+  // misc: bias buffers [2 tiles][2 bufs][128] floats, then barriers
+  static constexpr int OFF_BIAS = OFF_MISC;
+  static constexpr int OFF_BAR = OFF_BIAS + 2 * 2 * kBN * 4;
+  static constexpr int NBAR = 2 /*q_full*/ + 4 * NS /*k/v full/empty*/ + 2 /*s_full*/ +
+                              2 /*p_full*/ + 2 /*o_done*/ + 4 /*bias*/ + 1 /*drain*/;
+  static constexpr int OFF_SCALARS = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_SCALARS + 64;
+  static constexpr int SMEM_ALLOC = BYTES + 1024;          // slack for 1024-B alignment
+};
+
+struct Bars {
+  uint64_t* q_full;    // [2]
+  uint64_t* k_full;    // [NS]
+  uint64_t* k_empty;   // [NS]
+  uint64_t* v_full;    // [NS]
+  uint64_t* v_empty;   // [NS]
+  uint64_t* s_full;    // [2]
+  uint64_t* p_full;    // [2]
+  uint64_t* o_done;    // [2]
+  uint64_t* bias_rdy;  // [2 tiles][2 bufs]
+  uint64_t* drain;     // [1]
+};
+
+template <int D>
+__device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
+  using C = FwdCfg<D>;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  Bars r;
+  r.q_full = b; b += 2;
+  r.k_full = b; b += C::NS;
+  r.k_empty = b; b += C::NS;
+  r.v_full = b; b += C::NS;
+  r.v_empty = b; b += C::NS;
+  r.s_full = b; b += 2;
+  r.p_full = b; b += 2;
+  r.o_done = b; b += 2;
+  r.bias_rdy = b; b += 4;
+  r.drain = b;
+  return r;
+}
+
+template <int D, bool CAUSAL, bool BIAS>
+__global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdBf16Args a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const Problem& p = a.p;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+
+  Bars bars = carve_bars<D>(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_SCALARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SCALARS + 4);
+  int* key_lo_s = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 8);
+  int* key_hi_s = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 12);
+  float* bias_buf = reinterpret_cast<float*>(smem + C::OFF_BIAS);
+  const WaitCtx wc{abort_flag, a.err};
+
+  // ---- which (query-tile pair, head): heaviest causal tiles first
+  const int BH = p.B * p.H;
+  const int n_pairs = (p.Nq + 2 * kBM - 1) / (2 * kBM);
+  const int pair = n_pairs - 1 - (int)(blockIdx.x / BH);
+  const int bh = (int)(blockIdx.x % BH);
+  const int b = bh / p.H;
+  const int q_base = pair * 2 * kBM;
+  const float* bias_row = BIAS ? a.bias + (size_t)b * p.Nk : nullptr;
+
+  // ---- set-up: barriers, TMEM, optional scan of the bias row
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.q_full[0], 1);
+    mbar_init(&bars.q_full[1], 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.p_full[t], kBM);
+      mbar_init(&bars.o_done[t], 1);
+      mbar_init(&bars.bias_rdy[2 * t + 0], kBM);
+      mbar_init(&bars.bias_rdy[2 * t + 1], kBM);
+    }
+    mbar_init(bars.drain, 1);
+    *abort_flag = 0;
+    *key_lo_s = p.Nk;
+    *key_hi_s = -1;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&a.tm_q);
+    tma_prefetch_desc(&a.tm_k);
+    tma_prefetch_desc(&a.tm_v);
+  }
+  __syncthreads();
+  if (BIAS) {
+    // first and last key with a finite bias; tiles outside are skipped
+    int lo = p.Nk, hi = -1;
+    for (int j = threadIdx.x; j < p.Nk; j += kThreads) {
+      if (bias_row[j] != -INFINITY) {
+        lo = min(lo, j);
+        hi = max(hi, j);
+      }
+    }
+    if (lo < p.Nk) atomicMin(key_lo_s, lo);
+    if (hi >= 0) atomicMax(key_hi_s, hi);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- key-tile ranges [lo, hi_t) of the two query tiles
+  const int n_kv = (p.Nk + kBN - 1) / kBN;
+  int lo = 0, hi_all = n_kv;
+  if (BIAS) {
+    const int klo = *key_lo_s, khi = *key_hi_s;
+    if (khi < 0) {
+      lo = hi_all = 0;
+    } else {
+      lo = klo / kBN;
+      hi_all = khi / kBN + 1;
+    }
+  }
+  int hi_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = q_base + t * kBM;
+    int h = hi_all;
+    if (r0 >= p.Nq) {
+      h = lo;   // tile past the last query row: inactive
+    } else if (CAUSAL) {
+      const long last_row = min(r0 + kBM - 1, p.Nq - 1);
+      const long lim = last_row + (long)p.Nk - p.Nq;
+      h = lim < 0 ? 0 : (int)min((long)hi_all, lim / kBN + 1);
+    }
+    hi_t[t] = max(h, lo);
+  }
+  const int hi = max(hi_t[0], hi_t[1]);
+  const bool any = hi > lo;
+
+  if (warp == 8) {
+    // ================================================================ TMA producer
+    if (lane == 0 && any) {
+      uint8_t* q_s = smem + C::OFF_Q;
+      for (int t = 0; t < 2; ++t) {
+        if (hi_t[t] <= lo) continue;
+        mbar_arrive_expect_tx(&bars.q_full[t], C::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(q_s + t * C::TILE + c * C::SUB, &a.tm_q, c * 64, q_base + t * kBM, bh,
+                      &bars.q_full[t]);
+      }
+      int nk = 0, nv = 0;   // K / V fills issued
+      for (int j = lo; j < hi; ++j) {
+        const int i = j - lo, s = i % C::NS, u = i / C::NS;
+        if (u > 0 && !wait1(&bars.k_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
+        mbar_arrive_expect_tx(&bars.k_full[s], C::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::SUB, &a.tm_k, c * 64, j * kBN, bh,
+                      &bars.k_full[s]);
+        ++nk;
+        if (u > 0 && !wait1(&bars.v_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
+        mbar_arrive_expect_tx(&bars.v_full[s], C::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::SUB, &a.tm_v, c * 64, j * kBN, bh,
+                      &bars.v_full[s]);
+        ++nv;
+      }
+      // Drain: wait (bounded, ignoring the abort flag) for the last fill of
+      // every stage, so that no copy is still landing when the CTA exits.
+      // In a normal run every fill has already been consumed and these
+      // return at once.
+      volatile int never = 0;
+      const WaitCtx wd{&never, a.err};
+      for (int i = max(0, nk - C::NS); i < nk; ++i)
+        wait1(&bars.k_full[i % C::NS], (i / C::NS) & 1, wd, ERR_WAIT_DRAIN);
+      for (int i = max(0, nv - C::NS); i < nv; ++i)
+        wait1(&bars.v_full[i % C::NS], (i / C::NS) & 1, wd, ERR_WAIT_DRAIN);
+      for (int t = 0; t < 2; ++t)
+        if (hi_t[t] > lo) wait1(&bars.q_full[t], 0, wd, ERR_WAIT_DRAIN);
+    }
+  } else if (warp == 9) {
+    // ================================================================ MMA issuer
+    if (lane == 0 && any) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
+      const uint32_t q_addr = smem_u32(smem + C::OFF_Q);
+      const uint32_t k_addr = smem_u32(smem + C::OFF_K);
+      const uint32_t v_addr = smem_u32(smem + C::OFF_V);
+      auto active = [&](int t, int j) { return j >= lo && j < hi_t[t]; };
+      auto issue_s = [&](int t, int s) {
+        const uint32_t qa = q_addr + t * C::TILE, ka = k_addr + s * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::SUB + (kk % 4) * 32;
+          mma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                 idesc_s, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int s, bool acc) {
+        const uint32_t va = v_addr + s * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
+                 sdesc_sw128(va + kk * 2048, C::SUB, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = true;
+      for (int t = 0; t < 2 && ok; ++t)
+        if (hi_t[t] > lo) ok = wait1(&bars.q_full[t], 0, wc, ERR_WAIT_MMA);
+      if (ok) ok = wait1(&bars.k_full[0], 0, wc, ERR_WAIT_MMA);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (active(t, lo)) {
+            issue_s(t, 0);
+            mma_commit(&bars.s_full[t]);
+          }
+        mma_commit(&bars.k_empty[0]);
+      }
+      for (int j = lo; j < hi && ok; ++j) {
+        const int i = j - lo, s = i % C::NS;
+        const int i1 = i + 1, s1 = i1 % C::NS;
+        if (!wait1(&bars.v_full[s], (i / C::NS) & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
+        bool k_next = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (active(t, j)) {
+            if (!wait1(&bars.p_full[t], i & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(t, s, i > 0);
+            mma_commit(&bars.o_done[t]);
+          }
+          if (j + 1 < hi && active(t, j + 1)) {
+            if (!k_next) {
+              if (!wait1(&bars.k_full[s1], (i1 / C::NS) & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_s(t, s1);
+            mma_commit(&bars.s_full[t]);
+          }
+        }
+        if (!ok) break;
+        if (j + 1 < hi) mma_commit(&bars.k_empty[s1]);
+        mma_commit(&bars.v_empty[s]);
+      }
+      // drain every MMA issued so far before TMEM is released
+      mma_commit(bars.drain);
+      volatile int never = 0;
+      wait1(bars.drain, 0, WaitCtx{&never, a.err}, ERR_WAIT_DRAIN);
+    }
+  } else {
+    // ================================================================ softmax
+    const int t = warp / 4;                 // query tile of this warpgroup
+    const int r = (warp % 4) * 32 + lane;   // row within the tile = TMEM lane
+    const int row_g = q_base + t * kBM + r;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    const uint32_t s_col = t * 128, o_col = 256 + t * D;
+    const float sl2 = p.scale * kLog2e;
+    const long off = (long)p.Nk - p.Nq;
+    // last visible key of this row / of the tile's first row (tile-uniform)
+    const long lim_row = CAUSAL ? min((long)row_g + off, (long)p.Nk - 1) : (long)p.Nk - 1;
+    const long lim_tile =
+        CAUSAL ? min((long)(q_base + t * kBM) + off, (long)p.Nk - 1) : (long)p.Nk - 1;
+    float m = -INFINITY, l = 0.f;
+    const int n_t = hi_t[t] - lo;
+    int i = 0;
+    for (; i < n_t; ++i) {
+      const int j = lo + i;
+      const int key0 = j * kBN;
+      if (BIAS) {
+        float* bb = bias_buf + (t * 2 + (i & 1)) * kBN;
+        const int kj = key0 + r;
+        bb[r] = kj < p.Nk ? bias_row[kj] * kLog2e : -INFINITY;
+        mbar_arrive(&bars.bias_rdy[t * 2 + (i & 1)]);
+        if (!wait_warp(&bars.bias_rdy[t * 2 + (i & 1)], (i >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) break;
+      }
+      if (!wait_warp(&bars.s_full[t], i & 1, wc, ERR_WAIT_SOFTMAX)) break;
+      tc_fence_after();
+      float s[kBN];
+      uint32_t* su = reinterpret_cast<uint32_t*>(s);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + c * 32, su + c * 32);
+      tmem_ld_wait();
+
+      const bool need_mask = (long)key0 + kBN - 1 > lim_tile;
+      const bool scaled = BIAS || need_mask;
+      float mx = -INFINITY;
+      if (scaled) {
+        const float* bb = bias_buf + (t * 2 + (i & 1)) * kBN;
+        const long lim_rel = lim_row - key0;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          float v = BIAS ? fmaf(s[c], sl2, bb[c]) : s[c] * sl2;
+          if (need_mask && c > lim_rel) v = -INFINITY;
+          s[c] = v;
+          mx = fmaxf(mx, v);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+        mx *= sl2;
+      }
+      // conditional move of the running max
+      float alpha = 1.f;
+      bool moved = false;
+      if (mx > m + kRescaleLog2 || (m == -INFINITY && mx > -INFINITY)) {
+        alpha = ex2(m - mx);   // m = -inf -> 0
+        moved = (m != -INFINITY);
+        m = mx;
+      }
+      const float mu = (m == -INFINITY) ? 0.f : m;
+      float psum = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < kBN; c0 += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float p0 = scaled ? ex2(s[c0 + c] - mu) : ex2(fmaf(s[c0 + c], sl2, -mu));
+          const float p1 = scaled ? ex2(s[c0 + c + 1] - mu) : ex2(fmaf(s[c0 + c + 1], sl2, -mu));
+          psum += p0 + p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(lane_base + s_col + c0 / 2, pk);
+      }
+      l = l * alpha + psum;
+      // rescale O if any row of this warp moved its max and O already holds data
+      if (__any_sync(0xffffffffu, moved) && i > 0) {
+        if (!wait_warp(&bars.o_done[t], (i - 1) & 1, wc, ERR_WAIT_SOFTMAX)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(lane_base + o_col + c0, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tmem_st32(lane_base + o_col + c0, ov);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[t]);
+    }
+    // ---- epilogue: O = O_acc / l (bf16), LSE = ln2 * (m + log2 l)
+    const bool completed = (i == n_t);
+    bool have_o = completed && n_t > 0;
+    if (have_o) {
+      if (!wait_warp(&bars.o_done[t], (n_t - 1) & 1, wc, ERR_WAIT_SOFTMAX)) have_o = false;
+      tc_fence_after();
+    }
+    if (completed) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t* orow = a.o + ((size_t)bh * p.Nq + row_g) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        if (have_o) {
+          tmem_ld32(lane_base + o_col + c0, ov);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          pk[c / 2] = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+        if (row_g < p.Nq) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (row_g < p.Nq)
+        a.lse[(size_t)bh * p.Nq + row_g] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool BIAS>
+cudaError_t launch_one(const FwdBf16Args& a, cudaStream_t s) {
+  using C = FwdCfg<D>;
+  auto kern = fwd_bf16_kernel<D, CAUSAL, BIAS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  const long BH = (long)a.p.B * a.p.H;
+  const long n_pairs = (a.p.Nq + 2 * kBM - 1) / (2 * kBM);
+  kern<<<(unsigned)(BH * n_pairs), kThreads, C::SMEM_ALLOC, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const FwdBf16Args& a, cudaStream_t s) {
+  const bool bias = a.bias != nullptr;
+  if (a.p.causal)
+    return bias ? launch_one<D, true, true>(a, s) : launch_one<D, true, false>(a, s);
+  return bias ? launch_one<D, false, true>(a, s) : launch_one<D, false, false>(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const FwdBf16Args& a, cudaStream_t s) {
+  return a.p.d == 64 ? launch_d<64>(a, s) : launch_d<128>(a, s);
+}
+
+}  // namespace fa

@@ -1,0 +1,123 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact IO-aware attention library.
+ *
+ * What the library computes (one attention head; every (b, h) is independent):
+ *
+ *   S = scale * Q K^T + bias          bias added after scaling
+ *   P = row-softmax(S),  O = P V
+ *   LSE_i = log(sum_j exp(S_ij))      natural log, one float per query row
+ *
+ * ("Understanding FlashAttention Pt 1", §0.2 Notation; "flash-attention"
+ * Part IV, Stages 6-7 for the O + fp32 LSE contract.) The forward streams K and
+ * V through on-chip tiles with the online-softmax recurrence ("Understanding
+ * FlashAttention Pt 1", §2.3-2.4; "FlashAttention, Explained", §10 and §13), so
+ * the Nq x Nk matrices S and P never reach device memory. The backward
+ * recomputes P from the saved LSE ("Understanding FlashAttention Pt 1", §3.6;
+ * "flash-attention", Part VII) and returns dQ, dK, dV.
+ *
+ * Layout. Every tensor is contiguous, row-major [B][H][N][d] with d innermost
+ * (PyTorch SDPA order, not flash-attn's [B][N][H][d]); LSE is [B][H][Nq] fp32;
+ * key_bias is [B][Nk] fp32, broadcast over heads and query rows.
+ *
+ * Masking.
+ *   - causal != 0: key j is visible to query i iff j <= i + (Nk - Nq)
+ *     (bottom-right alignment; the plain lower triangle when Nq == Nk);
+ *   - key_bias[b][j] = -INFINITY masks key j of batch b;
+ *   - a query row with no visible key gets O = 0 and LSE = -INFINITY
+ *     ("flash-attention", Part VI: fully masked rows give zeros, not NaN).
+ *
+ * Pointers. q, k, v, o, lse, dO, dq, dk, dv, key_bias and the workspace are
+ * DEVICE pointers owned by the caller; the library keeps none of them after a
+ * call returns and allocates no device memory per call. q, k, v, o, dO, dq,
+ * dk, dv must be 16-byte aligned; key_bias and lse 4-byte aligned.
+ *
+ * Streams and errors. Every call validates its arguments on the host before
+ * any launch and returns a status without synchronising; the work is queued
+ * on `stream` (a cudaStream_t; NULL = the legacy default stream). Launch
+ * failures map to FA_ERR_CUDA. Device-side failures (a bounded wait inside a
+ * kernel that timed out) are reported by fa_get_last_device_error.
+ * Calls on distinct streams may run concurrently.
+ *
+ * Supported: dtype FA_DTYPE_BF16 with d in {64, 128} (forward and backward);
+ * dtype FA_DTYPE_FP32 with d in {64, 128} (forward only; fp32 arithmetic).
+ * Nq, Nk >= 1, B, H >= 1, B * H < 2^31, Nq, Nk < 2^31 / d. Other values
+ * return FA_ERR_UNSUPPORTED or FA_ERR_INVALID_ARG.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, bad workspace */
+    FA_ERR_UNSUPPORTED = 2,   /* valid request outside what is implemented (d, dtype) */
+    FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    FA_ERR_DEVICE = 4         /* a kernel reported a device-side timeout */
+} fa_status;
+
+typedef enum {
+    FA_DTYPE_BF16 = 0,
+    FA_DTYPE_FP32 = 1
+} fa_dtype;
+
+/*
+ * Forward. Writes o [B,H,Nq,d] (dtype) and lse [B,H,Nq] (fp32, natural log).
+ * key_bias may be NULL (no bias). scale is applied to Q K^T before the bias
+ * (1/sqrt(d) for standard attention). lse may be NULL for the fp32 path only
+ * if the caller does not need it; the bf16 path always writes it.
+ * Computes: tiling + online softmax ("FlashAttention, Explained", §13; the
+ * query-tile-outer order of §20); causal tile skipping ("Understanding
+ * FlashAttention Pt 1", §3.5).
+ */
+fa_status fa_fwd(const void *q, const void *k, const void *v, const float *key_bias,
+                 void *o, float *lse,
+                 int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                 fa_dtype dtype, void *stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: D = rowsum(dO o O) as fp32
+ * [B,H,Nq] followed by an fp32 dQ accumulator [B,H,Nq,d], each 256-byte
+ * aligned. Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d);
+
+/*
+ * Backward. Given q, k, v, the o and lse written by fa_fwd with the same
+ * arguments, and dO (dtype, [B,H,Nq,d]), writes dq, dk, dv (dtype). The result
+ * is undefined if o/lse come from a different call. workspace must hold
+ * fa_bwd_workspace_size(...) bytes and be 256-byte aligned; its contents on
+ * entry do not matter. dQ is accumulated across key tiles with atomic adds,
+ * so dq may differ in the last bits between runs; dk and dv are
+ * deterministic.
+ * Computes: D_i = rowsum(dO_i o O_i), then per key tile: recompute S and
+ * P = exp(S - LSE), dV += P^T dO, dP = dO V^T, dS = P o (dP - D),
+ * dQ += scale dS K, dK += scale dS^T Q ("Understanding FlashAttention Pt 1",
+ * §3.6; "FlashAttention, Explained", §17; "flash-attention", Part VII).
+ */
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                 const float *lse, const void *dO,
+                 void *dq, void *dk, void *dv, const float *key_bias,
+                 int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                 fa_dtype dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *fa_status_string(fa_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word. Returns FA_ERR_DEVICE if any kernel since the last call gave up on a
+ * bounded wait (its outputs are then invalid), FA_ERR_CUDA if the
+ * synchronisation itself failed, FA_OK otherwise.
+ */
+fa_status fa_get_last_device_error(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

@@ -1,0 +1,115 @@
+"""CPU-side checks of the C ABI: the library builds, loads without a GPU,
+exports every entry point include/fa.h declares, and rejects bad arguments on
+the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_io_aware_03_gb300 as fa
+from exact_io_aware_03_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load()
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names.update(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string",
+              "fa_get_last_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert fa.fa_status_string(s).startswith("FA_")
+    assert fa.fa_status_string(99) == "unknown fa_status"
+
+
+def test_workspace_size(lib):
+    B, H, Nq, Nk, d = 4, 16, 4096, 4096, 128
+    rows = B * H * Nq
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_size(B, H, Nq, Nk, d) == r256(rows * 4) + r256(rows * d * 4)
+    assert fa.fa_bwd_workspace_size(0, 1, 1, 1, 64) == 0
+    assert fa.fa_bwd_workspace_size(1, 1, 3, 1, 64) == 256 + 768
+
+
+FAKE = 1 << 20          # 16-byte aligned, never dereferenced: rejected before any launch
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nk=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),          # bf16 path always writes LSE
+    (dict(k=FAKE + 8), fa.FA_ERR_INVALID_ARG),        # misaligned
+    (dict(key_bias=FAKE + 2), fa.FA_ERR_INVALID_ARG),
+    (dict(B=1 << 16, H=1 << 15), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=1 << 25), fa.FA_ERR_INVALID_ARG),        # Nq * d overflows 31 bits
+])
+def test_fwd_rejects_bad_arguments_on_host(lib, args, expect):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, key_bias=None, o=FAKE, lse=FAKE, B=1, H=1, Nq=16, Nk=16,
+             d=64, scale=0.125, causal=0, dtype=fa.FA_DTYPE_BF16, stream=None)
+    a.update(args)
+    assert fa.fa_fwd(**a) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(dtype=fa.FA_DTYPE_FP32), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(workspace=None), fa.FA_ERR_INVALID_ARG),
+    (dict(workspace=FAKE + 16), fa.FA_ERR_INVALID_ARG),   # not 256-byte aligned
+    (dict(workspace_bytes=100), fa.FA_ERR_INVALID_ARG),
+    (dict(dO=None), fa.FA_ERR_INVALID_ARG),
+    (dict(dv=FAKE + 4), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=FAKE + 2), fa.FA_ERR_INVALID_ARG),
+])
+def test_bwd_rejects_bad_arguments_on_host(lib, args, expect):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dO=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             key_bias=None, B=1, H=1, Nq=16, Nk=16, d=64, scale=0.125, causal=1,
+             dtype=fa.FA_DTYPE_BF16, workspace=FAKE, workspace_bytes=1 << 20, stream=None)
+    a.update(args)
+    assert fa.fa_bwd(**a) == expect
+
+
+def test_binding_refuses_to_run_without_the_library(tmp_path):
+    import importlib
+    mod = importlib.import_module("exact_io_aware_03_gb300")
+    saved = mod._lib
+    try:
+        mod._lib = None
+        with pytest.raises(ImportError):
+            mod.load(str(tmp_path / "missing.so"))
+    finally:
+        mod._lib = saved

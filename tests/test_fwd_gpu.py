@@ -1,0 +1,162 @@
+"""GPU parity of the forward (fa_fwd through the C ABI) against the fp64 oracle.
+
+Small problems are compared element by element in full; they span several
+128-row / 128-key tiles and ragged tails. The full-size workloads are
+compared on sampled rows the oracle computes one by one, plus properties that
+hold at any size (finite outputs, no writes outside the outputs).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_03_gb300 as fa
+import oracle
+import workloads
+from parity import Guarded, compare, compare_lse
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from exact_io_aware_03_gb300 import build
+    build.build()
+    fa.load()
+    torch.cuda.init()
+
+
+def run_fwd(q, k, v, bias, causal, scale):
+    """Inputs on the CPU; returns (O, LSE) on the CPU, checking guard bands."""
+    dev = "cuda"
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    bd = None if bias is None else bias.to(dev)
+    o = Guarded(q.shape, q.dtype)
+    lse = Guarded(q.shape[:3], torch.float32)
+    fa.fwd(qd, kd, vd, key_bias=bd, causal=causal, scale=scale, out=o.t, lse=lse.t)
+    fa.check_device_error()
+    o.check("O")
+    lse.check("LSE")
+    return o.t.cpu(), lse.t.cpu()
+
+
+def make(B, H, Nq, Nk, d, dtype=torch.bfloat16, seed=0, bias=None):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H, Nq, d, generator=g).to(dtype)
+    k = torch.randn(B, H, Nk, d, generator=g).to(dtype)
+    v = torch.randn(B, H, Nk, d, generator=g).to(dtype)
+    b = None
+    if bias == "pad":
+        L = torch.randint(1, Nk + 1, (B,), generator=g)
+        b = torch.zeros(B, Nk)
+        b[torch.arange(Nk)[None, :] >= L[:, None]] = -math.inf
+    elif bias == "finite":
+        b = torch.randn(B, Nk, generator=g)
+        b[:, ::7] = -math.inf
+    elif bias == "all_masked_first_batch":
+        b = torch.randn(B, Nk, generator=g)
+        b[0] = -math.inf
+    return q, k, v, b
+
+
+SMALL = [
+    # B, H, Nq, Nk, d, causal, bias
+    (1, 2, 256, 256, 128, False, None),
+    (1, 2, 256, 256, 128, True, None),
+    (2, 3, 384, 384, 64, True, None),
+    (1, 2, 300, 517, 64, False, None),        # ragged query and key tails
+    (2, 1, 300, 517, 128, True, None),        # Nq < Nk, bottom-right causal
+    (1, 2, 700, 190, 128, True, None),        # Nq > Nk: leading rows see no key
+    (2, 2, 129, 1000, 128, False, "pad"),     # key padding
+    (2, 2, 200, 333, 64, True, "finite"),     # finite bias + causal
+    (2, 1, 130, 260, 128, False, "all_masked_first_batch"),
+    (1, 1, 1, 1, 64, False, None),            # degenerate sizes
+    (1, 1, 1, 300, 128, True, None),
+    (3, 1, 257, 1, 128, False, None),
+    (1, 1, 64, 4096, 128, False, None),       # many key tiles: ring wrap-around
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal,bias", SMALL)
+def test_fwd_bf16_small_full_parity(B, H, Nq, Nk, d, causal, bias):
+    q, k, v, b = make(B, H, Nq, Nk, d, seed=B * 1000 + Nq + Nk, bias=bias)
+    scale = d ** -0.5
+    o, lse = run_fwd(q, k, v, b, causal, scale)
+    o_ref, lse_ref = oracle.fwd(q, k, v, bias=b, scale=scale, causal=causal)
+    tag = "(%d,%d,%d,%d,%d,causal=%s,bias=%s)" % (B, H, Nq, Nk, d, causal, bias)
+    compare("O", o, o_ref, extra=tag)
+    compare_lse(lse, lse_ref, extra=tag)
+    dead = np.isneginf(lse_ref)
+    if dead.any():   # rows with no visible key are exactly zero
+        assert bool((o.double().numpy()[dead] == 0).all())
+
+
+def test_fwd_bf16_large_magnitude_rescaling():
+    # scores of magnitude ~100s force the running max to move many times
+    q, k, v, _ = make(1, 2, 256, 1024, 128, seed=5)
+    q = (q.float() * 6).to(torch.bfloat16)
+    k = (k.float() * 5).to(torch.bfloat16)
+    for causal in (False, True):
+        o, lse = run_fwd(q, k, v, None, causal, 128 ** -0.5)
+        o_ref, lse_ref = oracle.fwd(q, k, v, scale=128 ** -0.5, causal=causal)
+        compare("O", o, o_ref)
+        compare_lse(lse, lse_ref)
+
+
+def test_fwd_bf16_increasing_scores_force_every_rescale():
+    # key j's score grows with j, so each new key tile raises the max by > 8 (log2)
+    Nk, d = 1024, 64
+    q = torch.zeros(1, 1, 128, d)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, 1, Nk, d)
+    k[0, 0, :, 0] = torch.arange(Nk, dtype=torch.float32) * 0.125
+    v = torch.randn(1, 1, Nk, d, generator=torch.Generator().manual_seed(3))
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    o, lse = run_fwd(q, k, v, None, False, 1.0)
+    o_ref, lse_ref = oracle.fwd(q, k, v, scale=1.0)
+    compare("O", o, o_ref)
+    compare_lse(lse, lse_ref)
+
+
+def test_fwd_f32_workload_full_parity():
+    w = workloads.WORKLOADS["f32_b1h1_n128_d64"]
+    x = workloads.make_inputs(w)
+    o, lse = run_fwd(x["q"], x["k"], x["v"], None, w.causal, w.scale)
+    o_ref, lse_ref = oracle.fwd(x["q"], x["k"], x["v"], scale=w.scale)
+    compare("O", o, o_ref, dtype="fp32")
+    assert float(np.abs(lse.double().numpy() - lse_ref).max()) <= 1e-5
+
+
+@pytest.mark.parametrize("Nq,Nk,d,causal,bias", [
+    (200, 333, 128, True, "finite"), (65, 70, 64, False, "pad"), (300, 130, 64, True, None)])
+def test_fwd_f32_small_full_parity(Nq, Nk, d, causal, bias):
+    q, k, v, b = make(2, 2, Nq, Nk, d, dtype=torch.float32, seed=11, bias=bias)
+    o, lse = run_fwd(q, k, v, b, causal, d ** -0.5)
+    o_ref, lse_ref = oracle.fwd(q, k, v, bias=b, scale=d ** -0.5, causal=causal)
+    compare("O", o, o_ref, dtype="fp32")
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isneginf(lse.numpy()), ~fin)
+    assert float(np.abs(lse.double().numpy()[fin] - lse_ref[fin]).max()) <= 1e-5
+
+
+FULL = [("bf16_b4h16_n2048_d64", False), ("bf16_b4h16_n2048_d64", True),
+        ("bf16_b2h32_n8192_d128_causal", True),
+        ("bf16_b4h16_n4096_d128_causal_bwd", True),
+        ("bf16_b8h16_q1024_k16384_d128_keypad", False)]
+
+
+@pytest.mark.parametrize("name,causal", FULL)
+def test_fwd_full_size_sampled_rows(name, causal):
+    w = workloads.WORKLOADS[name]
+    x = workloads.make_inputs(w, with_dO=False)
+    o, lse = run_fwd(x["q"], x["k"], x["v"], x["bias"], causal, w.scale)
+    heads, rows = workloads.sample_rows(w, 96)
+    o_ref, lse_ref = oracle.fwd_rows(x["q"], x["k"], x["v"], x["bias"], heads, rows,
+                                     scale=w.scale, causal=causal)
+    H = w.H
+    o_s = torch.stack([o[h // H, h % H, r] for h, r in zip(heads, rows)])
+    l_s = torch.stack([lse[h // H, h % H, r] for h, r in zip(heads, rows)])
+    compare("O[sampled]", o_s, o_ref, extra=name)
+    compare_lse(l_s, lse_ref, extra=name)
+    assert bool(torch.isfinite(o.float()).all())

@@ -1,0 +1,447 @@
+#!/usr/bin/env python
+"""Throughput of exact attention forward + backward on GB300.
+
+One step = the whole hot path on one batch: fa_fwd (O, LSE) then fa_bwd
+(preprocess, main loop, dQ conversion) on the causal d=128 workload
+B=4, H=16, Nq=Nk=4096 (bf16, seeded N(0,1) inputs). The metric is TFLOP/s with
+the convention forward = 4*B*H*Nq*Nk*d, backward = 2.5 x forward, both halved
+for causal.
+
+Prints ONE JSON line (rank 0). Under torchrun every rank runs its own replica
+of the workload on its own GPU (different seed) with no data exchange; the
+process group is used only for the barrier and the max-over-ranks timing.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+WORKLOAD = "bf16_b4h16_n4096_d128_causal_bwd"
+FWD_EXTRA = "bf16_b2h32_n8192_d128_causal"
+METRIC = "attention fwd/bwd TFLOP/s (bf16, causal, d=128) and % of GB300 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def flops(w):
+    f = 4.0 * w.B * w.H * w.Nq * w.Nk * w.d * (0.5 if w.causal else 1.0)
+    return f, (2.5 * f if w.backward else 0.0)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_sample(w, n_rows_total, seed_offset=0):
+    """Time the fp64 oracle on a bounded sample of workload w: `n_rows_total`
+    query rows spread over as many heads as there are oracle threads, each
+    head's rows processed on its own thread (forward rows, then their full
+    backward contributions). Returns (seconds, conventional flops, description)."""
+    import concurrent.futures
+
+    import numpy as np
+    import torch
+
+    import oracle
+
+    cores = oracle.num_threads()
+    per_thread = max(1, n_rows_total // max(1, min(cores, w.B * w.H)))
+    rows_per_head = min(w.Nq, per_thread)
+    n_heads = max(1, min(w.B * w.H, -(-n_rows_total // rows_per_head)))
+    key = (w.name, n_heads)
+    if key not in _ORACLE_INPUTS:
+        x = workloads.make_inputs(w.with_(B=1, H=n_heads), seed=w.seed + 777, with_dO=True)
+        heads = []
+        for h in range(n_heads):
+            f = lambda t: np.ascontiguousarray(t[0, h].to(torch.float64).numpy())
+            heads.append((f(x["q"]), f(x["k"]), f(x["v"]), f(x["dO"])))
+        bias = None if x["bias"] is None else np.ascontiguousarray(x["bias"][0].double().numpy())
+        _ORACLE_INPUTS[key] = (heads, bias)
+    heads, bias = _ORACLE_INPUTS[key]
+    rng = np.random.default_rng(seed_offset)
+    rows = [np.sort(rng.choice(w.Nq, size=min(rows_per_head, w.Nq), replace=False))
+            for _ in range(n_heads)]
+    # conventional flops of the sampled rows: 4*vis*d forward + 10*vis*d backward
+    conv = 0.0
+    for r in rows:
+        if w.causal:
+            vis = np.minimum(r + (w.Nk - w.Nq) + 1, w.Nk).clip(min=0)
+        else:
+            vis = np.full(r.shape, w.Nk)
+        conv += float(vis.sum()) * w.d * (4.0 + (10.0 if w.backward else 0.0))
+
+    def work(h):
+        qh, kh, vh, dOh = heads[h]
+        oracle.fwd_head_rows(qh, kh, vh, bias, rows[h], w.scale, w.causal)
+        if w.backward:
+            oracle.bwd_head_rows(qh, kh, vh, bias, dOh, rows[h], w.scale, w.causal)
+
+    threads = max(1, min(cores, n_heads))
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(work, range(n_heads)))
+    dt = time.perf_counter() - t0
+    desc = ("%d query rows (%d per head) of %d heads of %s: forward rows + their full "
+            "backward contributions, fp64, one thread per head, %d threads" %
+            (sum(len(r) for r in rows), len(rows[0]), n_heads, w.name, threads))
+    return dt, conv, desc, threads
+
+
+def calibrated_oracle(w, budget_s, seed_offset=0):
+    """Pick a sample size so that one oracle sample takes about budget_s seconds."""
+    import oracle
+    cores = oracle.num_threads()
+    probe = 16
+    dt, conv, _, nh = oracle_sample(w, probe * max(1, min(cores, w.B * w.H)), seed_offset)
+    per_row = dt / probe          # seconds per row on one head-thread (heads run in parallel)
+    return int(max(1.0, budget_s / max(per_row, 1e-6))) * nh
+
+
+def cpu_baseline(w, budget_s=12.0):
+    n_rows = calibrated_oracle(w, budget_s / 4)
+    dt, conv, desc, nh = oracle_sample(w, n_rows)
+    for i in range(3):   # grow the sample until it takes about budget_s
+        if dt >= 0.6 * budget_s or n_rows >= w.B * w.H * w.Nq:
+            break
+        n_rows = max(nh, int(n_rows * min(8.0, budget_s / max(dt, 1e-3))))
+        dt, conv, desc, nh = oracle_sample(w, n_rows, seed_offset=1 + i)
+    return {"value": conv / dt / 1e12, "unit": UNIT, "cores": nh, "kind": "oracle",
+            "sample": desc, "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = workloads.WORKLOADS[WORKLOAD]
+    total_budget = 150.0
+    per_step = max(0.5, total_budget / max(1, args.steps + args.warmup))
+    n_rows = calibrated_oracle(w, per_step)
+    dt, _, _, _ = oracle_sample(w, n_rows)
+    n_rows = max(1, int(n_rows * per_step / max(dt, 1e-3)))
+    for i in range(args.warmup):
+        oracle_sample(w, n_rows, seed_offset=i)
+    times, convs = [], []
+    desc = ""
+    nh = 1
+    for i in range(args.steps):
+        dt, conv, desc, nh = oracle_sample(w, n_rows, seed_offset=100 + i)
+        times.append(dt)
+        convs.append(conv)
+    value = sum(convs) / sum(times) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk,
+                       "d": w.d, "causal": w.causal},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nh, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import exact_io_aware_03_gb300 as fa
+    from exact_io_aware_03_gb300 import build as fa_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        fa_build.build()
+    if world > 1:
+        dist.barrier()
+    fa.load()
+
+    w = workloads.WORKLOADS[WORKLOAD]
+    f_fwd, f_bwd = flops(w)
+    x = workloads.make_inputs(w, with_dO=True, seed=w.seed + rank)
+    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(causal=w.causal, scale=w.scale)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fwd(q, k, v, out=o, lse=lse, **kw)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.bwd(q, k, v, o, lse, dO, workspace=ws, dq=dq, dk=dk, dv=dv, stage="preprocess", **kw)
+        if ev is not None:
+            ev[2].record(stream)
+        fa.bwd(q, k, v, o, lse, dO, workspace=ws, dq=dq, dk=dk, dv=dv, stage="main", **kw)
+        if ev is not None:
+            ev[3].record(stream)
+        fa.bwd(q, k, v, o, lse, dO, workspace=ws, dq=dq, dk=dk, dv=dv, stage="postprocess", **kw)
+        if ev is not None:
+            ev[4].record(stream)
+
+    launches_per_step = 4   # fwd, bwd preprocess, bwd main, bwd postprocess
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    fa.check_device_error(dev)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    fa.check_device_error(dev)
+    ms_total = t_start.elapsed_time(t_end)
+    parts = {n: [e[j].elapsed_time(e[j + 1]) for e in evs]
+             for j, n in enumerate(["fwd", "bwd_preprocess", "bwd_main", "bwd_postprocess"])}
+    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = (f_fwd + f_bwd) * world / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API: pinned host inputs in, results out
+    e2e_steps = max(3, min(args.steps, 20))
+    host_in = {n: x[n].pin_memory() for n in ("q", "k", "v", "dO")}
+    host_out = {"o": torch.empty_like(o, device="cpu").pin_memory(),
+                "lse": torch.empty_like(lse, device="cpu").pin_memory(),
+                "dq": torch.empty_like(dq, device="cpu").pin_memory(),
+                "dk": torch.empty_like(dk, device="cpu").pin_memory(),
+                "dv": torch.empty_like(dv, device="cpu").pin_memory()}
+    dev_in = {"q": q, "k": k, "v": v, "dO": dO}
+    dev_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        fa.fwd(q, k, v, out=o, lse=lse, **kw)
+        fa.bwd(q, k, v, o, lse, dO, workspace=ws, dq=dq, dk=dk, dv=dv, **kw)
+        for n, t in host_out.items():
+            t.copy_(dev_out[n], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    fa.check_device_error(dev)
+    te = torch.tensor([a0.elapsed_time(a1) / e2e_steps], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = (f_fwd + f_bwd) * world / (float(te.item()) * 1e-3) / 1e12
+
+    # ---- extra forward-only measurement on the long-context causal workload
+    extras = {}
+    if not args.no_extras:
+        we = workloads.WORKLOADS[FWD_EXTRA]
+        g = torch.Generator(device=dev).manual_seed(we.seed + rank)
+        qe, ke, ve = (torch.randn((we.B, we.H, we.Nq, we.d), generator=g, device=dev,
+                                  dtype=torch.bfloat16) for _ in range(3))
+        oe = torch.empty_like(qe)
+        le = torch.empty(qe.shape[:3], dtype=torch.float32, device=dev)
+        for _ in range(3):
+            fa.fwd(qe, ke, ve, out=oe, lse=le, causal=True, scale=we.scale)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e = 20
+        b0.record(stream)
+        for _ in range(n_e):
+            fa.fwd(qe, ke, ve, out=oe, lse=le, causal=True, scale=we.scale)
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        fa.check_device_error(dev)
+        ms_e = b0.elapsed_time(b1) / n_e
+        extras[FWD_EXTRA + "_fwd_tflops"] = flops(we)[0] / (ms_e * 1e-3) / 1e12
+        extras[FWD_EXTRA + "_fwd_ms"] = ms_e
+        del qe, ke, ve, oe, le
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    med = {n: statistics.median(v) for n, v in parts.items()}
+    bwd_main_tflops = f_bwd / (med["bwd_main"] * 1e-3) / 1e12
+    fwd_tflops = f_fwd / (med["fwd"] * 1e-3) / 1e12
+    # dominant kernel: the one with the largest share of the step
+    dom = max(("fwd", "bwd_main"), key=lambda n: med[n])
+    dom_flops = f_bwd if dom == "bwd_main" else f_fwd
+    mean_dom = sum(parts[dom]) / len(parts[dom])
+    achieved = dom_flops / (mean_dom * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    traffic = TRAFFIC_BYTES.get(dom)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_source": "%s (sustained bf16 dense)" % peak_src,
+                "frac_of_burst_peak": achieved / peaks.get("bf16_tflops", 1900.0)}
+    cpu = cpu_baseline(w) if world == 1 else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": w.causal, "step": "fa_fwd + fa_bwd",
+                   "flop_convention": "fwd 4*B*H*Nq*Nk*d, bwd 2.5x fwd, halved for causal",
+                   "l2": "inputs larger than L2 (q,k,v,dO 64 MiB each + outputs), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "parts_ms_median": med,
+        "fwd_tflops": fwd_tflops,
+        "bwd_main_tflops": bwd_main_tflops,
+        "extras": extras,
+        "clocks": clk.summary(),
+        "peaks_source": peak_src,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+# DRAM bytes per launch of the dominant kernels from an ncu capture, or None
+# when the kernel changed since the counters were taken.
+TRAFFIC_BYTES = {"fwd": None, "bwd_main": None}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the forward-only long-context measurement")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

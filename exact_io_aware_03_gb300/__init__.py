@@ -46,9 +46,11 @@ def load(path=None):
     lib.fa_fwd.restype = cint
     lib.fa_bwd_workspace_size.argtypes = [cint] * 5
     lib.fa_bwd_workspace_size.restype = csz
-    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint,
-                           cf, cint, cint, vp, csz, vp]
-    lib.fa_bwd.restype = cint
+    for name in ("fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess"):
+        f = getattr(lib, name)
+        f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint,
+                      cf, cint, cint, vp, csz, vp]
+        f.restype = cint
     lib.fa_status_string.argtypes = [cint]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_get_last_device_error.argtypes = [vp]
@@ -68,6 +70,24 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale, ca
            workspace, workspace_bytes, stream):
     return load().fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale,
                          causal, dtype, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_preprocess(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale, causal,
+                      dtype, workspace, workspace_bytes, stream):
+    return load().fa_bwd_preprocess(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d,
+                                    scale, causal, dtype, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_main(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale, causal,
+                dtype, workspace, workspace_bytes, stream):
+    return load().fa_bwd_main(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale,
+                              causal, dtype, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_postprocess(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale, causal,
+                       dtype, workspace, workspace_bytes, stream):
+    return load().fa_bwd_postprocess(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d,
+                                     scale, causal, dtype, workspace, workspace_bytes, stream)
 
 
 def fa_bwd_workspace_size(B, H, Nq, Nk, d):
@@ -134,8 +154,12 @@ def fwd(q, k, v, key_bias=None, causal=False, scale=None, out=None, lse=None):
 
 
 def bwd(q, k, v, o, lse, dO, key_bias=None, causal=False, scale=None, workspace=None,
-        dq=None, dk=None, dv=None):
-    """dQ, dK, dV (q's dtype) for CUDA tensors; o and lse from ``fwd`` on the same inputs."""
+        dq=None, dk=None, dv=None, stage=None):
+    """dQ, dK, dV (q's dtype) for CUDA tensors; o and lse from ``fwd`` on the same inputs.
+
+    stage: None runs the whole backward (fa_bwd); "preprocess", "main" or
+    "postprocess" runs only that launch (the three in order equal fa_bwd).
+    """
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (dO, "dO")):
         _check(t, n)
@@ -149,13 +173,15 @@ def bwd(q, k, v, o, lse, dO, key_bias=None, causal=False, scale=None, workspace=
     ws_bytes = fa_bwd_workspace_size(B, H, Nq, Nk, d)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    fn = {None: fa_bwd, "preprocess": fa_bwd_preprocess, "main": fa_bwd_main,
+          "postprocess": fa_bwd_postprocess}[stage]
     with torch.cuda.device(q.device):
-        st = fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+        st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
                     _ptr(dk), _ptr(dv), _ptr(key_bias), B, H, Nq, Nk, d, float(scale),
                     int(bool(causal)), _dtype_code(q), _ptr(workspace), workspace.numel(),
                     _stream(q))
     if st != FA_OK:
-        raise FaError(st, "fa_bwd")
+        raise FaError(st, fn.__name__)
     return dq, dk, dv
 
 

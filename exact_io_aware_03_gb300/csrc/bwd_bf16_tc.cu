@@ -1,8 +1,506 @@
-// bf16 backward (placeholder until the tensor-core backward lands).
+// bf16 backward on the 5th-generation tensor cores.
+//
+// Three launches on the caller's stream ("flash-attention", Part VII;
+// "FlashAttention, Explained", §17; "Understanding FlashAttention Pt 1", §3.6):
+//
+//  1. bwd_pre: D_i = rowsum(dO_i o O_i) in fp32, LSE converted to the base-2
+//     domain (a fully masked row's -inf becomes +inf so that its recomputed
+//     probabilities are exactly 0), and the fp32 dQ accumulator zeroed.
+//  2. bwd_main: one CTA per (128-key tile j, head), key/value tile resident in
+//     shared memory; it walks the 128-row query tiles i that can see tile j
+//     (causal: only i at or below the bottom-right diagonal) and per tile
+//       S^T  = K_j Q_i^T                      tcgen05 -> TMEM (lane = key)
+//       P^T  = exp2(S^T*c + bias - LSE_i)     recomputed from the saved LSE
+//       dP^T = V_j dO_i^T                      tcgen05 -> TMEM
+//       dV_j += P^T dO_i                       A = P^T read from TMEM
+//       dS^T = P^T o (dP^T - D_i)              -> TMEM (bf16) and shared memory
+//       dK_j += dS^T Q_i                       A = dS^T read from TMEM
+//       dQ_i  = dS K_j                         A = dS from shared memory
+//     dQ_i is added (fp32 vector reductions) into the accumulator, because
+//     several key tiles contribute to the same query rows; dK_j and dV_j stay
+//     in TMEM until the last query tile and are written once, scaled.
+//  3. bwd_post: dQ = bf16(accumulator).
+//
+// Warp roles of bwd_main (320 threads): warps 0-7 are two warpgroups that
+// split the query columns of every tile; they compute P^T (kept in fp32
+// registers) and dS^T (thread = key = TMEM lane), read dQ_i out of TMEM
+// (thread = query row) and reduce it into global memory, and write dK/dV at
+// the end; warp 8 issues TMA loads; warp 9 allocates TMEM and issues the MMAs.
+// TMEM (512 columns): S^T [0,128), then per half h of the query columns the
+// packed bf16 P^T in [64h, 64h+32) and dS^T in [64h+32, 64h+64) (each
+// warpgroup overwrites only scores it has already read); dP^T then dQ
+// [128,256); dV [256,256+D); dK [256+D,256+2D).
+#include <cmath>
+#include <cstdint>
+
 #include "fa_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace fa {
+namespace {
 
-cudaError_t launch_bwd_bf16(const BwdBf16Args&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kThreads = 320;
+constexpr int kT = 128;   // keys per key tile = rows per query tile
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------ preprocess
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
+                                                      const uint16_t* __restrict__ dO,
+                                                      const float* __restrict__ lse,
+                                                      float* __restrict__ Dv,
+                                                      float* __restrict__ lse2,
+                                                      float* __restrict__ dq_acc, long rows) {
+  constexpr int LPR = D / 8;          // lanes per row, 8 bf16 (16 B) per lane
+  constexpr int RPW = 32 / LPR;       // rows per warp step
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, li = lane % LPR;
+  const long warp_g = ((long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const long nwarps = ((long)gridDim.x * blockDim.x) / 32;
+  for (long r0 = warp_g * RPW; r0 < rows; r0 += nwarps * RPW) {
+    const long row = r0 + sub;
+    float acc = 0.f;
+    if (row < rows) {
+      const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[li];
+      const uint4 g = reinterpret_cast<const uint4*>(dO + row * D)[li];
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(gv[e] << 16), acc);
+        acc = fmaf(__uint_as_float(av[e] & 0xffff0000u), __uint_as_float(gv[e] & 0xffff0000u),
+                   acc);
+      }
+      float4* z = reinterpret_cast<float4*>(dq_acc + row * D);
+      z[2 * li] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[2 * li + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int w = LPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (row < rows && li == 0) {
+      Dv[row] = acc;
+      const float L = lse[row];
+      lse2[row] = (L == -INFINITY) ? INFINITY : L * kLog2e;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ post
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ acc,
+                                                       uint16_t* __restrict__ dq, long n4) {
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (long)gridDim.x * blockDim.x) {
+    const float4 v = reinterpret_cast<const float4*>(acc)[i];
+    reinterpret_cast<uint2*>(dq)[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+// ------------------------------------------------------------------ main
+template <int D>
+struct BwdCfg {
+  static constexpr int TILE = kT * D * 2;     // bf16 [128][D]
+  static constexpr int SUB = kT * 128;        // one 64-column box
+  static constexpr int DS_BYTES = kT * kT * 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;         // [2 stages]
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;    // [2 stages]
+  static constexpr int OFF_DS = OFF_DO + 2 * TILE;
+  // [2 warpgroups][2 bufs] {lse2[64], D[64]}
+  static constexpr int OFF_STAT = OFF_DS + DS_BYTES;
+  static constexpr int OFF_BAR = OFF_STAT + 2 * 2 * kT * 4;
+  static constexpr int NBAR = 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 4 + 1;
+  static constexpr int OFF_SCALARS = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_SCALARS + 32;
+};
+
+struct BwdBars {
+  uint64_t* kv_full;   // [1]
+  uint64_t* q_full;    // [2]  Q_i and dO_i of a stage
+  uint64_t* q_empty;   // [2]
+  uint64_t* s_full;    // S^T done
+  uint64_t* dp_full;   // dP^T done
+  uint64_t* p_full;    // P^T in TMEM (128 arrivals)
+  uint64_t* ds_full;   // dS^T in TMEM + smem (128 arrivals)
+  uint64_t* dq_full;   // dQ_i done (and everything before it)
+  uint64_t* dq_empty;  // dQ_i read out of TMEM (128 arrivals)
+  uint64_t* stat_rdy;  // [2 warpgroups][2 bufs] lse2/D staged (128 arrivals)
+  uint64_t* drain;
+};
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int D, bool CAUSAL, bool BIAS>
+__global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdBf16Args a) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Problem& p = a.p;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+
+  uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  BwdBars bars;
+  bars.kv_full = bb; bb += 1;
+  bars.q_full = bb; bb += 2;
+  bars.q_empty = bb; bb += 2;
+  bars.s_full = bb; bb += 1;
+  bars.dp_full = bb; bb += 1;
+  bars.p_full = bb; bb += 1;
+  bars.ds_full = bb; bb += 1;
+  bars.dq_full = bb; bb += 1;
+  bars.dq_empty = bb; bb += 1;
+  bars.stat_rdy = bb; bb += 4;
+  bars.drain = bb;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_SCALARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SCALARS + 4);
+  int* any_key = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 8);
+  const WaitCtx wc{abort_flag, a.err};
+
+  const int BH = p.B * p.H;
+  const int jt = (int)(blockIdx.x / BH);   // key tile; low j first = most query tiles (causal)
+  const int bh = (int)(blockIdx.x % BH);
+  const int b = bh / p.H;
+  const int key0 = jt * kT;
+  const long off = (long)p.Nk - p.Nq;
+
+  // ---- query tiles [i0, i1) that can see this key tile
+  const int n_qt = (p.Nq + kT - 1) / kT;
+  int i0 = 0;
+  if (CAUSAL) {
+    // smallest i with i*128 + 127 + off >= key0
+    const long need = (long)key0 - off - (kT - 1);
+    i0 = need <= 0 ? 0 : (int)min((long)n_qt, (need + kT - 1) / kT);
+  }
+  const int i1 = n_qt;
+
+  if (threadIdx.x == 0) {
+    if ((smem_u32(smem) & 1023u) != 0) atomicOr(a.err, ERR_WAIT_DRAIN);   // layout invariant
+    mbar_init(bars.kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.q_full[s], 1);
+      mbar_init(&bars.q_empty[s], 1);
+    }
+    for (int s = 0; s < 4; ++s) mbar_init(&bars.stat_rdy[s], kT);
+    mbar_init(bars.s_full, 1);
+    mbar_init(bars.dp_full, 1);
+    mbar_init(bars.p_full, 2 * kT);
+    mbar_init(bars.ds_full, 2 * kT);
+    mbar_init(bars.dq_full, 1);
+    mbar_init(bars.dq_empty, 2 * kT);
+    mbar_init(bars.drain, 1);
+    *abort_flag = (smem_u32(smem) & 1023u) != 0;
+    *any_key = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  // per-key bias (log2 domain); keys past Nk are masked
+  float kb = -INFINITY;
+  if (warp < 8) {
+    const int key = key0 + (threadIdx.x & 127);
+    if (key < p.Nk) kb = BIAS ? a.bias[(size_t)b * p.Nk + key] * kLog2e : 0.f;
+    if (kb != -INFINITY) *any_key = 1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n = (*any_key && !*abort_flag) ? max(0, i1 - i0) : 0;
+
+  if (warp == 8) {
+    // ================================================================ TMA producer
+    if (lane == 0 && n > 0) {
+      mbar_arrive_expect_tx(bars.kv_full, 2 * C::TILE);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, key0, bh, bars.kv_full);
+        tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, key0, bh, bars.kv_full);
+      }
+      int issued = 0;
+      for (int it = 0; it < n; ++it) {
+        const int s = it & 1, u = it >> 1;
+        if (u > 0 && !wait1(&bars.q_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
+        const int q0 = (i0 + it) * kT;
+        mbar_arrive_expect_tx(&bars.q_full[s], 2 * C::TILE);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * C::SUB, &a.tm_q, c * 64, q0, bh,
+                      &bars.q_full[s]);
+          tma_load_3d(smem + C::OFF_DO + s * C::TILE + c * C::SUB, &a.tm_do, c * 64, q0, bh,
+                      &bars.q_full[s]);
+        }
+        ++issued;
+      }
+      const WaitCtx wd{abort_flag, a.err, true};
+      wait1(bars.kv_full, 0, wd, ERR_WAIT_DRAIN);
+      for (int it = max(0, issued - 2); it < issued; ++it)
+        wait1(&bars.q_full[it & 1], (it >> 1) & 1, wd, ERR_WAIT_DRAIN);
+    }
+  } else if (warp == 9) {
+    // ================================================================ MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);    // S^T, dP^T
+      constexpr uint32_t id_acc = idesc_bf16_f32(kT, D, false, true);    // dV, dK (A in TMEM)
+      constexpr uint32_t id_dq = idesc_bf16_f32(kT, D, true, true);      // dQ (A = dS, MN-major)
+      const uint32_t k_a = smem_u32(smem + C::OFF_K), v_a = smem_u32(smem + C::OFF_V);
+      const uint32_t ds_a = smem_u32(smem + C::OFF_DS);
+      const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
+      bool ok = wait1(bars.kv_full, 0, wc, ERR_WAIT_MMA);
+      for (int it = 0; it < n && ok; ++it) {
+        const int s = it & 1;
+        const uint32_t q_a = smem_u32(smem + C::OFF_Q + s * C::TILE);
+        const uint32_t do_a = smem_u32(smem + C::OFF_DO + s * C::TILE);
+        if (!(ok = wait1(&bars.q_full[s], (it >> 1) & 1, wc, ERR_WAIT_MMA))) break;
+        tc_fence_after();
+        // S^T = K Q^T (both K-major, 128-byte rows per 64-column box)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
+          mma_ss(t_s, sdesc_sw128(k_a + o, 16, 1024), sdesc_sw128(q_a + o, 16, 1024), id_s, kk > 0);
+        }
+        mma_commit(bars.s_full);
+        // dP^T = V dO^T, once dQ of the previous tile has left TMEM
+        if (it > 0 && !(ok = wait1(bars.dq_empty, (it - 1) & 1, wc, ERR_WAIT_MMA))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
+          mma_ss(t_dp, sdesc_sw128(v_a + o, 16, 1024), sdesc_sw128(do_a + o, 16, 1024), id_s,
+                 kk > 0);
+        }
+        mma_commit(bars.dp_full);
+        // dV += P^T dO  (P^T packed bf16: query columns [0,64) in TMEM columns
+        // [0,32), [64,128) in [64,96))
+        if (!(ok = wait1(bars.p_full, it & 1, wc, ERR_WAIT_MMA))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8,
+                 sdesc_sw128(do_a + kk * 2048, C::SUB, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q ; dQ = dS K
+        if (!(ok = wait1(bars.ds_full, it & 1, wc, ERR_WAIT_MMA))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ts(t_dk, t_s + (kk / 4) * 64 + 32 + (kk % 4) * 8,
+                 sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ss(t_dp, sdesc_sw128(ds_a + kk * 2048, C::SUB, 1024),
+                 sdesc_sw128(k_a + kk * 2048, C::SUB, 1024), id_dq, kk > 0 ? 1u : 0u);
+        mma_commit(bars.dq_full);
+        mma_commit(&bars.q_empty[s]);
+      }
+      mma_commit(bars.drain);
+      wait1(bars.drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
+    }
+  } else {
+    // ================================================================ warps 0-7
+    // Two warpgroups share the 128 keys (thread = key = TMEM lane) and split the
+    // 128 query columns of each tile: warpgroup h handles columns [64h, 64h+64)
+    // of S^T / P^T / dP^T / dS^T, and columns [h*D/2, (h+1)*D/2) of dQ, dK, dV.
+    const int h = warp / 4;
+    const int r = (warp % 4) * 32 + lane;            // key within the tile = TMEM lane
+    const int key = key0 + r;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    const float sl2 = p.scale * kLog2e;
+    const float* lse2g = a.lse;    // base-2 LSE (workspace copy written by bwd_pre)
+    const float* Dg = a.D;
+    float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);
+    uint8_t* ds_s = smem + C::OFF_DS;
+    constexpr int HD = D / 2;      // dQ / dK / dV columns per warpgroup
+
+    // dQ of query tile `it` (TMEM lane = query row): read this warpgroup's
+    // columns, hand the TMEM region back, then reduce into the accumulator.
+    auto dq_readout = [&](int it) -> bool {
+      if (!wait_warp(bars.dq_full, it & 1, wc, ERR_WAIT_EPILOGUE)) return false;
+      tc_fence_after();
+      uint32_t x[HD];
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) tmem_ld32(lane_base + 128 + h * HD + c * 32, x + c * 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(bars.dq_empty);
+      const int row = (i0 + it) * kT + r;
+      if (row < p.Nq) {
+        float* dst = a.dq_acc + ((size_t)bh * p.Nq + row) * D + h * HD;
+#pragma unroll
+        for (int c = 0; c < HD; c += 4)
+          red_add_v4(dst + c, __uint_as_float(x[c]) * p.scale, __uint_as_float(x[c + 1]) * p.scale,
+                     __uint_as_float(x[c + 2]) * p.scale, __uint_as_float(x[c + 3]) * p.scale);
+      }
+      return true;
+    };
+
+    int it = 0;
+    bool ok = true;
+    for (; it < n; ++it) {
+      const int q0 = (i0 + it) * kT;
+      if (it > 0 && !(ok = dq_readout(it - 1))) break;
+      // stage base-2 LSE (first 64) and D (last 64) of this warpgroup's query rows
+      float* st = stat + (h * 2 + (it & 1)) * kT;
+      {
+        const int row = q0 + h * 64 + (r & 63);
+        const bool in = row < p.Nq;
+        st[r] = r < 64 ? (in ? lse2g[(size_t)bh * p.Nq + row] : INFINITY)
+                       : (in ? Dg[(size_t)bh * p.Nq + row] : 0.f);
+      }
+      mbar_arrive(&bars.stat_rdy[h * 2 + (it & 1)]);
+      if (!(ok = wait_warp(&bars.stat_rdy[h * 2 + (it & 1)], (it >> 1) & 1, wc, ERR_WAIT_SOFTMAX)))
+        break;
+      if (!(ok = wait_warp(bars.s_full, it & 1, wc, ERR_WAIT_SOFTMAX))) break;
+      tc_fence_after();
+      // P^T = exp2(S^T * scale*log2e + bias - LSE2), masked -> 0; kept in fp32 for dS
+      const bool need_mask = CAUSAL && ((long)q0 + off < (long)key0 + kT - 1);
+      const long thr = (long)key - off - q0 - h * 64;   // local column < thr -> masked
+      float P[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32];
+        tmem_ld32(lane_base + h * 64 + c * 32, sv);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x = fmaf(__uint_as_float(sv[e]), sl2, kb) - st[c * 32 + e];
+          if (need_mask && c * 32 + e < thr) x = -INFINITY;
+          P[c * 32 + e] = ex2(x);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) pk[e / 2] = pack_bf16x2(P[c * 32 + e], P[c * 32 + e + 1]);
+        tmem_st16(lane_base + h * 64 + c * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bars.p_full);
+
+      // dS^T = P^T o (dP^T - D), to TMEM (A of dK) and shared memory (A of dQ)
+      if (!(ok = wait_warp(bars.dp_full, it & 1, wc, ERR_WAIT_SOFTMAX))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dpv[32];
+        tmem_ld32(lane_base + 128 + h * 64 + c * 32, dpv);
+        tmem_ld_wait();
+        uint32_t dsk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float d0 = P[c * 32 + e] * (__uint_as_float(dpv[e]) - st[64 + c * 32 + e]);
+          const float d1 =
+              P[c * 32 + e + 1] * (__uint_as_float(dpv[e + 1]) - st[64 + c * 32 + e + 1]);
+          dsk[e / 2] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(lane_base + h * 64 + 32 + c * 16, dsk);
+        // row = key of a 128-byte-swizzled box holding query columns [64h, 64h+64)
+        uint8_t* rowp = ds_s + h * C::SUB + r * 128;
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          const int chunk = (c * 4 + v4) ^ (r & 7);
+          *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+              make_uint4(dsk[4 * v4], dsk[4 * v4 + 1], dsk[4 * v4 + 2], dsk[4 * v4 + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bars.ds_full);
+    }
+    if (ok && n > 0) ok = dq_readout(n - 1);   // also: every MMA of this CTA has completed
+    // ---- dK, dV of this key tile (this warpgroup's half of the columns)
+    if (ok && it == n) {
+      const bool have = n > 0;
+      const size_t base = ((size_t)bh * p.Nk + key) * D + h * HD;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {   // 0: dV, 1: dK
+        uint16_t* dst = (which ? a.dk : a.dv) + base;
+        const float mul = which ? p.scale : 1.f;
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t x[32];
+          if (have) {
+            tmem_ld32(lane_base + 256 + which * D + h * HD + c0, x);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = 0u;
+          }
+          uint32_t pkd[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]) * mul, __uint_as_float(x[e + 1]) * mul);
+          if (key < p.Nk) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              d4[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool BIAS>
+cudaError_t launch_main(const BwdBf16Args& a, cudaStream_t s) {
+  using C = BwdCfg<D>;
+  auto kern = bwd_main_kernel<D, CAUSAL, BIAS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
+  if (e != cudaSuccess) return e;
+  const long BH = (long)a.p.B * a.p.H;
+  const long n_kt = (a.p.Nk + kT - 1) / kT;
+  kern<<<(unsigned)(BH * n_kt), kThreads, C::BYTES, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const BwdBf16Args& a, cudaStream_t s, unsigned stages) {
+  const long rows = (long)a.p.B * a.p.H * a.p.Nq;
+  cudaError_t e = cudaSuccess;
+  if (stages & BWD_PRE) {
+    constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
+    const long blocks = min((rows + kRowsPerBlock - 1) / kRowsPerBlock, (long)a.num_sms * 8);
+    bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a.o, a.dO, a.lse, a.D, a.lse2, a.dq_acc,
+                                                      rows);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (stages & BWD_MAIN) {
+    BwdBf16Args m = a;
+    m.lse = a.lse2;   // the main kernel reads the base-2 LSE written by the preprocess
+    const bool bias = a.bias != nullptr;
+    if (a.p.causal)
+      e = bias ? launch_main<D, true, true>(m, s) : launch_main<D, true, false>(m, s);
+    else
+      e = bias ? launch_main<D, false, true>(m, s) : launch_main<D, false, false>(m, s);
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & BWD_POST) {
+    const long n4 = rows * D / 4;
+    const long blocks = min((n4 + 255) / 256, (long)a.num_sms * 8);
+    bwd_post_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.dq_acc, a.dq, n4);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16(const BwdBf16Args& a, cudaStream_t s, unsigned stages) {
+  return a.p.d == 64 ? launch_d<64>(a, s, stages) : launch_d<128>(a, s, stages);
+}
 
 }  // namespace fa

@@ -139,13 +139,19 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, const float* key_b
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
   const size_t rows = (size_t)B * H * Nq;
-  return round256(rows * 4) + round256(rows * (size_t)d * 4);
+  return 2 * round256(rows * 4) + round256(rows * (size_t)d * 4);
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                 const void* dO, void* dq, void* dk, void* dv, const float* key_bias, int B,
-                 int H, int Nq, int Nk, int d, float scale, int causal, fa_dtype dtype,
-                 void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation and argument set-up shared by fa_bwd and its three stages.
+fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                     const float* key_bias, int B, int H, int Nq, int Nk, int d, float scale,
+                     int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                     void* stream, unsigned stages) {
   fa_status st = check_problem(B, H, Nq, Nk, d, scale, dtype);
   if (st != FA_OK) return st;
   if (dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
@@ -162,25 +168,73 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   std::memset(&a, 0, sizeof(a));
   a.p = fa::Problem{B, H, Nq, Nk, d, scale, causal ? 1 : 0};
   const int BH = B * H;
-  if ((st = make_map(&a.tm_q, q, BH, Nq, d)) != FA_OK) return st;
-  if ((st = make_map(&a.tm_k, k, BH, Nk, d)) != FA_OK) return st;
-  if ((st = make_map(&a.tm_v, v, BH, Nk, d)) != FA_OK) return st;
-  if ((st = make_map(&a.tm_do, dO, BH, Nq, d)) != FA_OK) return st;
+  if (stages & fa::BWD_MAIN) {
+    if ((st = make_map(&a.tm_q, q, BH, Nq, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_k, k, BH, Nk, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_v, v, BH, Nk, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_do, dO, BH, Nq, d)) != FA_OK) return st;
+  }
   a.o = static_cast<const uint16_t*>(o);
   a.dO = static_cast<const uint16_t*>(dO);
   a.lse = lse;
   a.bias = key_bias;
   const size_t rows = (size_t)BH * Nq;
-  a.D = static_cast<float*>(workspace);
-  a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * 4));
+  char* ws = static_cast<char*>(workspace);
+  a.D = reinterpret_cast<float*>(ws);
+  a.lse2 = reinterpret_cast<float*>(ws + round256(rows * 4));
+  a.dq_acc = reinterpret_cast<float*>(ws + 2 * round256(rows * 4));
   a.dq = static_cast<uint16_t*>(dq);
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
   if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
-  cudaError_t e = fa::launch_bwd_bf16(a, static_cast<cudaStream_t>(stream));
-  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&a.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  cudaError_t e = fa::launch_bwd_bf16(a, static_cast<cudaStream_t>(stream), stages);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+}  // namespace
+
+extern "C" {
+
+#define FA_BWD_ARGS                                                                        \
+  q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale, causal, dtype, workspace, \
+      workspace_bytes, stream
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv, const float* key_bias, int B,
+                 int H, int Nq, int Nk, int d, float scale, int causal, fa_dtype dtype,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_common(FA_BWD_ARGS, fa::BWD_PRE | fa::BWD_MAIN | fa::BWD_POST);
+}
+
+fa_status fa_bwd_preprocess(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                            const float* key_bias, int B, int H, int Nq, int Nk, int d,
+                            float scale, int causal, fa_dtype dtype, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  return bwd_common(FA_BWD_ARGS, fa::BWD_PRE);
+}
+
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                      const float* key_bias, int B, int H, int Nq, int Nk, int d, float scale,
+                      int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  return bwd_common(FA_BWD_ARGS, fa::BWD_MAIN);
+}
+
+fa_status fa_bwd_postprocess(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                             const float* key_bias, int B, int H, int Nq, int Nk, int d,
+                             float scale, int causal, fa_dtype dtype, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return bwd_common(FA_BWD_ARGS, fa::BWD_POST);
+}
+
+#undef FA_BWD_ARGS
 
 fa_status fa_get_last_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;

@@ -42,15 +42,20 @@ struct BwdBf16Args {
   const float* lse;
   const float* bias;
   float* D;            // workspace: rowsum(dO o O), [B][H][Nq]
+  float* lse2;         // workspace: LSE * log2(e) (+inf for fully masked rows)
   float* dq_acc;       // workspace: fp32 dQ accumulator [B][H][Nq][d]
   uint16_t* dq;
   uint16_t* dk;
   uint16_t* dv;
   uint32_t* err;
+  int num_sms;
 };
 
 cudaError_t launch_fwd_f32(const FwdF32Args& a, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const FwdBf16Args& a, cudaStream_t s);
-cudaError_t launch_bwd_bf16(const BwdBf16Args& a, cudaStream_t s);
+// Backward stages (bit mask): D / base-2 LSE / zeroed dQ accumulator; the
+// tensor-core main loop; the dQ conversion.
+enum : unsigned { BWD_PRE = 1u, BWD_MAIN = 2u, BWD_POST = 4u };
+cudaError_t launch_bwd_bf16(const BwdBf16Args& a, cudaStream_t s, unsigned stages);
 
 }  // namespace fa

@@ -243,8 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       // every stage, so that no copy is still landing when the CTA exits.
       // In a normal run every fill has already been consumed and these
       // return at once.
-      volatile int never = 0;
-      const WaitCtx wd{&never, a.err};
+      const WaitCtx wd{abort_flag, a.err, true};
       for (int i = max(0, nk - C::NS); i < nk; ++i)
         wait1(&bars.k_full[i % C::NS], (i / C::NS) & 1, wd, ERR_WAIT_DRAIN);
       for (int i = max(0, nv - C::NS); i < nv; ++i)
@@ -319,8 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       }
       // drain every MMA issued so far before TMEM is released
       mma_commit(bars.drain);
-      volatile int never = 0;
-      wait1(bars.drain, 0, WaitCtx{&never, a.err}, ERR_WAIT_DRAIN);
+      wait1(bars.drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
     }
   } else {
     // ================================================================ softmax

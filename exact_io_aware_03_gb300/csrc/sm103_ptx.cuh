@@ -65,11 +65,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Shared state every bounded wait consults.
+// Shared state every bounded wait consults. A non-zero device error word
+// (another CTA already gave up) also ends a wait, so that after one timeout the
+// remaining CTAs of the grid stop quickly instead of each waiting out its own.
 struct WaitCtx {
   volatile int* abort_flag;   // CTA-wide, in shared memory
   uint32_t* err_word;         // device error word (global)
+  bool drain = false;         // drain waits ignore aborts: only the time limit ends them
 };
+
+__device__ __forceinline__ bool grid_failed(const uint32_t* err_word) {
+  return *reinterpret_cast<const volatile uint32_t*>(err_word) != 0u;
+}
 
 __device__ __forceinline__ void raise_abort(const WaitCtx& w, uint32_t code) {
   *w.abort_flag = 1;
@@ -84,7 +91,11 @@ __device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, const Wait
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
-      if (*w.abort_flag) return false;
+      if (!w.drain && *w.abort_flag) return false;
+      if (!w.drain && grid_failed(w.err_word)) {
+        *w.abort_flag = 1;
+        return false;
+      }
       if (globaltimer() - t0 > FA_WAIT_TIMEOUT_NS) {
         raise_abort(w, code);
         return false;
@@ -106,6 +117,9 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const 
       if (lane_id() == 0) {
         if (t0 == 0) t0 = globaltimer();
         if (*w.abort_flag) {
+          stop = 1;
+        } else if (grid_failed(w.err_word)) {
+          *w.abort_flag = 1;
           stop = 1;
         } else if (globaltimer() - t0 > FA_WAIT_TIMEOUT_NS) {
           raise_abort(w, code);

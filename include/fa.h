@@ -35,7 +35,9 @@
  * any launch and returns a status without synchronising; the work is queued
  * on `stream` (a cudaStream_t; NULL = the legacy default stream). Launch
  * failures map to FA_ERR_CUDA. Device-side failures (a bounded wait inside a
- * kernel that timed out) are reported by fa_get_last_device_error.
+ * kernel that timed out) are reported by fa_get_last_device_error; the error
+ * is sticky: until that call clears it, later launches on the device stop at
+ * their first slow wait, and their outputs are invalid too.
  * Calls on distinct streams may run concurrently.
  *
  * Supported: dtype FA_DTYPE_BF16 with d in {64, 128} (forward and backward);
@@ -81,8 +83,9 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, const float *key_b
 
 /*
  * Bytes of device workspace fa_bwd needs: D = rowsum(dO o O) as fp32
- * [B,H,Nq] followed by an fp32 dQ accumulator [B,H,Nq,d], each 256-byte
- * aligned. Returns 0 for invalid sizes.
+ * [B,H,Nq], the LSE rescaled to base 2 as fp32 [B,H,Nq], and an fp32 dQ
+ * accumulator [B,H,Nq,d], each starting on a 256-byte boundary.
+ * Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d);
 
@@ -104,6 +107,36 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  void *dq, void *dk, void *dv, const float *key_bias,
                  int B, int H, int Nq, int Nk, int d, float scale, int causal,
                  fa_dtype dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The three launches of fa_bwd, one per call, with fa_bwd's arguments and
+ * validation; calling them in this order on one stream is equivalent to
+ * fa_bwd ("flash-attention", Part VII: a preprocess launch, then the main
+ * backward launch):
+ *   fa_bwd_preprocess   D = rowsum(dO o O), base-2 LSE, zeroed dQ accumulator
+ *                       (reads o, lse, dO; writes the workspace);
+ *   fa_bwd_main         recompute P per tile, dK and dV (written to dk, dv),
+ *                       dQ reduced into the workspace accumulator;
+ *   fa_bwd_postprocess  dq = bf16(dQ accumulator).
+ * Useful to time or schedule the stages separately.
+ */
+fa_status fa_bwd_preprocess(const void *q, const void *k, const void *v, const void *o,
+                            const float *lse, const void *dO,
+                            void *dq, void *dk, void *dv, const float *key_bias,
+                            int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                            fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                            void *stream);
+fa_status fa_bwd_main(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dO,
+                      void *dq, void *dk, void *dv, const float *key_bias,
+                      int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                      fa_dtype dtype, void *workspace, size_t workspace_bytes, void *stream);
+fa_status fa_bwd_postprocess(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dO,
+                             void *dq, void *dk, void *dv, const float *key_bias,
+                             int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                             fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                             void *stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *fa_status_string(fa_status s);

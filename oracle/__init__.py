@@ -40,6 +40,12 @@ def _load():
         for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_bwd,
                   lib.oracle_bwd_dq_rows):
             f.restype = ctypes.c_int
+        lib.oracle_bwd_head_rows.argtypes = [dp, dp, dp, dp, dp, ip, ci, dp, dp, dp,
+                                             ci, ci, ci, cd, ci, dp]
+        lib.oracle_bwd_head_rows.restype = None
+        lib.oracle_fwd_head_rows.argtypes = [dp, dp, dp, dp, ip, ci, dp, dp, ci, ci, ci, cd,
+                                             ci, dp]
+        lib.oracle_fwd_head_rows.restype = None
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -159,18 +165,20 @@ def bwd(q, k, v, bias, dO, scale=None, causal=False):
 
 
 def bwd_heads(q, k, v, bias, dO, heads, scale=None, causal=False):
-    """dQ, dK, dV of whole heads (flat indices), each [n_heads, N, d]."""
-    B, H, Nq, d = q.shape
-    out = []
-    for bh in heads:
-        b = bh // H
-        sl = [_head_slice(t, bh, H) for t in (q, k, v)]
-        bb = None if bias is None else _f64(bias[b][None])
-        dq, dk, dv = bwd(sl[0], sl[1], sl[2], bb, _head_slice(dO, bh, H),
-                         scale=scale, causal=causal)
-        out.append((dq[0, 0], dk[0, 0], dv[0, 0]))
-    return (np.stack([o[0] for o in out]), np.stack([o[1] for o in out]),
-            np.stack([o[2] for o in out]))
+    """dQ, dK, dV of whole heads (flat indices b*H+h), each [n_heads, N, d].
+
+    The selected heads are stacked as a batch of single-head problems so that
+    they run in parallel (one OpenMP task per head).
+    """
+    H = q.shape[1]
+    heads = [int(h) for h in heads]
+
+    def sel(x):
+        return np.stack([_f64(x[bh // H, bh % H]) for bh in heads])[:, None]
+
+    bb = None if bias is None else np.stack([_f64(bias[bh // H]) for bh in heads])
+    dq, dk, dv = bwd(sel(q), sel(k), sel(v), bb, sel(dO), scale=scale, causal=causal)
+    return dq[:, 0], dk[:, 0], dv[:, 0]
 
 
 def bwd_dq_rows(q, k, v, bias, dO, heads, rows, scale=None, causal=False):
@@ -198,3 +206,44 @@ def bwd_dq_rows(q, k, v, bias, dO, heads, rows, scale=None, causal=False):
             raise MemoryError("oracle_bwd_dq_rows: scratch allocation failed")
         dq[idx] = out
     return dq
+
+
+def bwd_head_rows(qh, kh, vh, bias_row, dOh, rows, scale, causal, dk=None, dv=None):
+    """Backward contributions of the given query rows of one head (float64 arrays
+    [N, d]; bias_row [Nk] or None), on the calling thread (releases the GIL).
+
+    Returns dq [len(rows), d] and the dK, dV contributions [Nk, d] of those rows
+    (accumulated into dk / dv when given). The same per-row work as ``bwd``.
+    """
+    lib = _load()
+    Nq, d = qh.shape
+    Nk = kh.shape[0]
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    dq = np.empty((rows.size, d))
+    dk = np.zeros((Nk, d)) if dk is None else dk
+    dv = np.zeros((Nk, d)) if dv is None else dv
+    scratch = np.empty(2 * max(Nk, 1))
+    lib.oracle_bwd_head_rows(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(bias_row), _ptr(dOh),
+                             rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), rows.size,
+                             _ptr(dq), _ptr(dk), _ptr(dv), Nq, Nk, d, float(scale),
+                             int(bool(causal)), _ptr(scratch))
+    return dq, dk, dv
+
+
+def fwd_head_rows(qh, kh, vh, bias_row, rows, scale, causal):
+    """O [len(rows), d] and LSE of the given query rows of one head (float64 [N, d]),
+    on the calling thread (releases the GIL)."""
+    lib = _load()
+    Nq, d = qh.shape
+    Nk = kh.shape[0]
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    n = rows.size
+    o = np.empty((n, d))
+    lse = np.empty(n)
+    scratch = np.empty(max(Nk, 1))
+    lib.oracle_fwd_head_rows(_ptr(np.ascontiguousarray(qh)), _ptr(np.ascontiguousarray(kh)),
+                             _ptr(np.ascontiguousarray(vh)), _ptr(bias_row),
+                             rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n,
+                             _ptr(o), _ptr(lse), Nq, Nk, d, float(scale), int(bool(causal)),
+                             _ptr(scratch))
+    return o, lse

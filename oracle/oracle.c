@@ -201,8 +201,9 @@ int oracle_fwd_rows(const double *q, const double *k, const double *v,
  * materialised in full, then its dS row is formed from the Jacobian and
  * scattered into dQ (row i), dK and dV (all keys).
  * dq [Nq][d] is written; dk, dv [Nk][d] must be zeroed by the caller.
- * If rows != NULL only those query rows are processed and only dq is written
- * (dq [nrows][d] in the order of rows); dk/dv may then be NULL.
+ * If rows != NULL only those query rows are processed: dq [nrows][d] is
+ * written in the order of rows, and, when dk and dv are not NULL, the
+ * contributions of exactly those rows are added into them.
  */
 static void bwd_head(const double *q, const double *k, const double *v,
                      const double *bias, const double *dO,
@@ -234,7 +235,7 @@ static void bwd_head(const double *q, const double *k, const double *v,
             double ds = p[j] * (dp[j] - rowdot);
             const double *kj = k + (size_t)j * d;
             for (int c = 0; c < d; ++c) dqi[c] += scale * ds * kj[c];
-            if (!rows) {
+            if (dk && dv) {
                 double *dkj = dk + (size_t)j * d, *dvj = dv + (size_t)j * d;
                 for (int c = 0; c < d; ++c) {
                     dkj[c] += scale * ds * qi[c];
@@ -312,6 +313,33 @@ int oracle_bwd_dq_rows(const double *q, const double *k, const double *v,
         free(dp);
     }
     return failed ? -1 : 0;
+}
+
+/*
+ * Backward contributions of selected query rows of ONE head, on the calling
+ * thread: dq [nrows][d] (complete rows of dQ), and the part of dK, dV
+ * ([Nk][d], accumulated into, caller zeroes them) that those rows produce.
+ * Summed over all rows this is oracle_bwd; used to time the oracle on a
+ * bounded sample of a workload.
+ */
+void oracle_bwd_head_rows(const double *q, const double *k, const double *v,
+                          const double *bias, const double *dO, const int *rows, int nrows,
+                          double *dq, double *dk, double *dv,
+                          int Nq, int Nk, int d, double scale, int causal,
+                          double *scratch /* 2 * Nk doubles */)
+{
+    bwd_head(q, k, v, bias, dO, dq, dk, dv, rows, nrows, Nq, Nk, d, scale, causal,
+             scratch, scratch + Nk);
+}
+
+/* Forward of selected query rows of ONE head, on the calling thread:
+ * o [nrows][d], lse [nrows]; scratch holds Nk doubles. */
+void oracle_fwd_head_rows(const double *q, const double *k, const double *v,
+                          const double *bias, const int *rows, int nrows,
+                          double *o, double *lse, int Nq, int Nk, int d, double scale,
+                          int causal, double *scratch)
+{
+    fwd_head_rows(q, k, v, bias, rows, 0, nrows, o, lse, Nq, Nk, d, scale, causal, scratch);
 }
 
 int oracle_num_threads(void)

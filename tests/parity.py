@@ -66,7 +66,8 @@ class Guarded:
         n = int(np.prod(shape))
         self.n = n
         self.buf = torch.empty(n + 2 * self.PAD, dtype=dtype, device=device)
-        self.sentinel = torch.tensor(-12345.0, dtype=dtype)
+        self.sentinel = torch.tensor(0xA5 if not dtype.is_floating_point else -12345.0,
+                                     dtype=dtype)
         self.buf.fill_(self.sentinel.item())
         self.t = self.buf[self.PAD:self.PAD + n].view(shape)
         if fill is not None:

@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string",
-              "fa_get_last_device_error"):
+              "fa_get_last_device_error", "fa_bwd_preprocess", "fa_bwd_main",
+              "fa_bwd_postprocess"):
         assert n in names
 
 
@@ -52,9 +53,9 @@ def test_workspace_size(lib):
     B, H, Nq, Nk, d = 4, 16, 4096, 4096, 128
     rows = B * H * Nq
     r256 = lambda x: (x + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_size(B, H, Nq, Nk, d) == r256(rows * 4) + r256(rows * d * 4)
+    assert fa.fa_bwd_workspace_size(B, H, Nq, Nk, d) == 2 * r256(rows * 4) + r256(rows * d * 4)
     assert fa.fa_bwd_workspace_size(0, 1, 1, 1, 64) == 0
-    assert fa.fa_bwd_workspace_size(1, 1, 3, 1, 64) == 256 + 768
+    assert fa.fa_bwd_workspace_size(1, 1, 3, 1, 64) == 2 * 256 + 768
 
 
 FAKE = 1 << 20          # 16-byte aligned, never dereferenced: rejected before any launch
@@ -95,12 +96,14 @@ def test_fwd_rejects_bad_arguments_on_host(lib, args, expect):
     (dict(dv=FAKE + 4), fa.FA_ERR_INVALID_ARG),
     (dict(lse=FAKE + 2), fa.FA_ERR_INVALID_ARG),
 ])
-def test_bwd_rejects_bad_arguments_on_host(lib, args, expect):
+@pytest.mark.parametrize("fn", ["fa_bwd", "fa_bwd_preprocess", "fa_bwd_main",
+                                "fa_bwd_postprocess"])
+def test_bwd_rejects_bad_arguments_on_host(lib, args, expect, fn):
     a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dO=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
              key_bias=None, B=1, H=1, Nq=16, Nk=16, d=64, scale=0.125, causal=1,
              dtype=fa.FA_DTYPE_BF16, workspace=FAKE, workspace_bytes=1 << 20, stream=None)
     a.update(args)
-    assert fa.fa_bwd(**a) == expect
+    assert getattr(fa, fn)(**a) == expect
 
 
 def test_binding_refuses_to_run_without_the_library(tmp_path):

@@ -386,3 +386,23 @@ def test_rowsum_identity_D():
     P = np.exp(s - lse[..., None])
     dP = np.einsum("bhid,bhjd->bhij", G, v)
     np.testing.assert_allclose((G * o).sum(-1), (P * dP).sum(-1), atol=1e-13)
+
+
+def test_row_sampled_backward_sums_to_full_backward():
+    B, H, Nq, Nk, d = 1, 1, 13, 17, 6
+    q, k, v, G = rand((B, H, Nq, d), 60), rand((B, H, Nk, d), 61), rand((B, H, Nk, d), 62), \
+        rand((B, H, Nq, d), 63)
+    bias = np.zeros((B, Nk))
+    bias[0, 15:] = -np.inf
+    dq, dk, dv = oracle.bwd(q, k, v, bias, G, scale=0.5, causal=True)
+    dk_acc, dv_acc = np.zeros((Nk, d)), np.zeros((Nk, d))
+    parts = [np.arange(0, 5), np.arange(5, 13)]
+    for rows in parts:
+        dqr, _, _ = oracle.bwd_head_rows(q[0, 0], k[0, 0], v[0, 0], bias[0], G[0, 0], rows, 0.5,
+                                         True, dk=dk_acc, dv=dv_acc)
+        np.testing.assert_allclose(dqr, dq[0, 0, rows], atol=1e-15)
+    np.testing.assert_allclose(dk_acc, dk[0, 0], atol=1e-14)
+    np.testing.assert_allclose(dv_acc, dv[0, 0], atol=1e-14)
+    o, l = oracle.fwd_head_rows(q[0, 0], k[0, 0], v[0, 0], bias[0], [3, 12], 0.5, True)
+    of, lf = oracle.fwd(q, k, v, bias=bias, scale=0.5, causal=True)
+    np.testing.assert_allclose(o, of[0, 0, [3, 12]], atol=1e-15)

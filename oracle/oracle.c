@@ -18,7 +18,8 @@
  * maximum m, then l = sum_j exp(s_j - m), then p_j = exp(s_j - m) / l.
  * Every query row is materialised in full (all Nk scores) before any of it is
  * used. The saved statistic is the natural-log log-sum-exp
- * LSE_i = m_i + ln(l_i) ("flash-attention", Part VI: "LSE = m2 + ln(l2)").
+ * LSE_i = m_i + ln(l_i) ("flash-attention", Part VI: its worked example adds
+ * the natural log of the final denominator to the final max).
  *
  * Masking:
  *  - key-padding bias: bias[b][j] is added to every score of key j in batch b;

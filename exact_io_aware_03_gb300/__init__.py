@@ -102,6 +102,25 @@ def fa_get_last_device_error(stream):
     return load().fa_get_last_device_error(stream)
 
 
+FA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale, causal,
+                   dtype, stream):
+    """fa_bwd without a workspace argument: the library's own fixed device
+    array (FA_NOALLOC_SCRATCH_BYTES) serves as the workspace, for callers that
+    cannot allocate device memory. Calls that overlap on the GPU race."""
+    lib = load()
+    f = lib.fa_bwd_noalloc
+    if f.restype is not ctypes.c_int or not f.argtypes:
+        vp, cint, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint, cf,
+                      cint, cint, vp]
+        f.restype = cint
+    return f(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale, causal, dtype,
+             stream)
+
+
 # ------------------------------------------------------------------ torch conveniences
 
 def _dtype_code(t):

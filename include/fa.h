@@ -138,6 +138,35 @@ fa_status fa_bwd_postprocess(const void *q, const void *k, const void *v, const 
                              fa_dtype dtype, void *workspace, size_t workspace_bytes,
                              void *stream);
 
+/*
+ * Size in bytes of the device array fa_bwd_noalloc uses as its workspace.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * fa_bwd_noalloc -- fa_bwd without a caller-provided workspace. (The pages
+ * have no counterpart: this is a convenience of this library.)
+ *
+ * For callers that cannot allocate device memory while attention runs (a
+ * runtime that plans all device memory ahead and passes kernels only their
+ * inputs and outputs, code running inside an allocator callback, a service
+ * that may not call cudaMalloc on its request path). The workspace comes from
+ * a fixed 32 MiB array in the library's device image, held by every GPU that
+ * loads the library until the process exits; nothing is allocated per call.
+ * Arguments, layout, results and error codes are those of fa_bwd, except:
+ *   - FA_ERR_UNSUPPORTED if fa_bwd_workspace_size(B, H, Nq, Nk, d) exceeds
+ *     FA_NOALLOC_SCRATCH_BYTES (checked before any launch);
+ *   - all calls share the array: calls that overlap on the GPU race and must
+ *     be serialised by the caller;
+ *   - the first call on a device looks up the array's address on that device
+ *     (the current one); make that first call before any stream capture.
+ */
+fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dO,
+                         void *dq, void *dk, void *dv, const float *key_bias,
+                         int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                         fa_dtype dtype, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *fa_status_string(fa_status s);
 

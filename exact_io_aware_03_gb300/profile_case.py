@@ -1,0 +1,63 @@
+"""Run the library's kernels on a named workload a few times, for profilers.
+
+    python -m exact_io_aware_03_gb300.profile_case --workload NAME [--pass fwd|bwd|both]
+                                                   [--iters N] [--causal 0|1]
+
+Inputs are the seeded synthetic tensors of `workloads.py`. Each iteration runs
+fa_fwd and/or fa_bwd once on the current stream; the script synchronises and
+checks the device error word at the end. Nothing is timed or compared: this
+is the small, self-contained command to put under `ncu`.
+"""
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main(argv=None):
+    import torch
+
+    import exact_io_aware_03_gb300 as fa
+    import workloads
+    from exact_io_aware_03_gb300 import build
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="bf16_b4h16_n4096_d128_causal_bwd",
+                    choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "both"], default="both")
+    ap.add_argument("--iters", type=int, default=2)
+    ap.add_argument("--causal", type=int, choices=[0, 1], default=None,
+                    help="override the workload's causal flag")
+    args = ap.parse_args(argv)
+
+    w = workloads.WORKLOADS[args.workload]
+    if args.causal is not None:
+        w = w.with_(causal=bool(args.causal))
+    build.build()
+    fa.load()
+    dev = torch.device("cuda", 0)
+    x = workloads.make_inputs(w, with_dO=True)
+    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
+    bias = None if x["bias"] is None else x["bias"].to(dev)
+    kw = dict(key_bias=bias, causal=w.causal, scale=w.scale)
+    o, lse = fa.fwd(q, k, v, **kw)
+    if w.dtype == "bf16":
+        ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d), dtype=torch.uint8,
+                         device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    for _ in range(args.iters):
+        if args.which in ("fwd", "both"):
+            fa.fwd(q, k, v, out=o, lse=lse, **kw)
+        if args.which in ("bwd", "both") and w.dtype == "bf16":
+            fa.bwd(q, k, v, o, lse, dO, workspace=ws, dq=dq, dk=dk, dv=dv, **kw)
+    torch.cuda.synchronize(dev)
+    fa.check_device_error(dev)
+    print("ok: %s %s x%d" % (w.name, args.which, args.iters))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

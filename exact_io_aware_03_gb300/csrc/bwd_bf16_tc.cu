@@ -13,10 +13,10 @@
 //       P^T  = exp2(S^T*c + bias - LSE_i)     recomputed from the saved LSE
 //       dP^T = V_j dO_i^T                      tcgen05 -> TMEM
 //       dV_j += P^T dO_i                       A = P^T read from TMEM
-//       dS^T = P^T o (dP^T - D_i)              -> TMEM (bf16) and shared memory
-//       dK_j += dS^T Q_i                       A = dS^T read from TMEM
+//       dS^T = P^T o (dP^T - D_i)              -> shared memory (bf16)
+//       dK_j += dS^T Q_i                       A = dS^T from shared memory
 //       dQ_i  = dS K_j                         A = dS from shared memory
-//     dQ_i is added (fp32 vector reductions) into the accumulator, because
+//     dQ_i is reduce-added (TMA bulk tensor reductions) into the accumulator, because
 //     several key tiles contribute to the same query rows; dK_j and dV_j stay
 //     in TMEM until the last query tile and are written once, scaled.
 //  3. bwd_post: dQ = bf16(accumulator).
@@ -27,9 +27,11 @@
 // (thread = query row) and reduce it into global memory, and write dK/dV at
 // the end; warp 8 issues TMA loads; warp 9 allocates TMEM and issues the MMAs.
 // TMEM (512 columns): S^T [0,128), then per half h of the query columns the
-// packed bf16 P^T in [64h, 64h+32) and dS^T in [64h+32, 64h+64) (each
-// warpgroup overwrites only scores it has already read); dP^T then dQ
-// [128,256); dV [256,256+D); dK [256+D,256+2D).
+// packed bf16 P^T in [64h, 64h+32) (each warpgroup overwrites only scores it
+// has already read); dP^T then dQ [128,256); dV [256,256+D); dK [256+D,256+2D).
+// dS^T goes to shared memory only: it is the A operand of both dK (K-major
+// view) and dQ (MN-major view), so the S^T columns are free as soon as dV has
+// read P^T, and S^T of the next tile overlaps dK and dQ of this one.
 #include <cmath>
 #include <cstdint>
 
@@ -127,14 +129,6 @@ struct BwdBars {
   uint64_t* drain;
 };
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a),
-               "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 template <int D, bool CAUSAL, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdBf16Args a) {
@@ -162,9 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   int* any_key = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 8);
   const WaitCtx wc{abort_flag, a.err};
 
-  const int BH = p.B * p.H;
-  const int jt = (int)(blockIdx.x / BH);   // key tile; low j first = most query tiles (causal)
-  const int bh = (int)(blockIdx.x % BH);
+  // Head-major order: the CTAs running together cover few heads, so their Q,
+  // dO and dQ accumulator stay in L2; within a head the low key tiles (the
+  // most query tiles under a causal mask) come first.
+  const int n_kt = (p.Nk + kT - 1) / kT;
+  const int bh = (int)(blockIdx.x / n_kt);
+  const int jt = (int)(blockIdx.x % n_kt);
   const int b = bh / p.H;
   const int key0 = jt * kT;
   const long off = (long)p.Nk - p.Nq;
@@ -247,25 +244,34 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // ================================================================ MMA issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);    // S^T, dP^T
-      constexpr uint32_t id_acc = idesc_bf16_f32(kT, D, false, true);    // dV, dK (A in TMEM)
+      constexpr uint32_t id_acc = idesc_bf16_f32(kT, D, false, true);    // dV, dK (A K-major)
       constexpr uint32_t id_dq = idesc_bf16_f32(kT, D, true, true);      // dQ (A = dS, MN-major)
       const uint32_t k_a = smem_u32(smem + C::OFF_K), v_a = smem_u32(smem + C::OFF_V);
       const uint32_t ds_a = smem_u32(smem + C::OFF_DS);
       const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
-      bool ok = wait1(bars.kv_full, 0, wc, ERR_WAIT_MMA);
-      for (int it = 0; it < n && ok; ++it) {
-        const int s = it & 1;
-        const uint32_t q_a = smem_u32(smem + C::OFF_Q + s * C::TILE);
-        const uint32_t do_a = smem_u32(smem + C::OFF_DO + s * C::TILE);
-        if (!(ok = wait1(&bars.q_full[s], (it >> 1) & 1, wc, ERR_WAIT_MMA))) break;
-        tc_fence_after();
-        // S^T = K Q^T (both K-major, 128-byte rows per 64-column box)
+      // S^T = K Q^T for query tile `it` (both K-major, 128-byte rows per box)
+      auto issue_s = [&](int it) {
+        const uint32_t q_a = smem_u32(smem + C::OFF_Q + (it & 1) * C::TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
           mma_ss(t_s, sdesc_sw128(k_a + o, 16, 1024), sdesc_sw128(q_a + o, 16, 1024), id_s, kk > 0);
         }
         mma_commit(bars.s_full);
+      };
+      // Issue order per query tile i:  dP(i) [after dQ(i-1) left TMEM],
+      // dV(i) [after P(i)], S(i+1) [the S columns are free once dV(i) has
+      // read P(i)], dK(i), dQ(i) [after dS(i)]. S(i+1) and the softmax of
+      // tile i+1 thus overlap dK(i) and dQ(i).
+      bool ok = wait1(bars.kv_full, 0, wc, ERR_WAIT_MMA);
+      if (ok && (ok = wait1(&bars.q_full[0], 0, wc, ERR_WAIT_MMA))) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int it = 0; it < n && ok; ++it) {
+        const int s = it & 1;
+        const uint32_t q_a = smem_u32(smem + C::OFF_Q + s * C::TILE);
+        const uint32_t do_a = smem_u32(smem + C::OFF_DO + s * C::TILE);
         // dP^T = V dO^T, once dQ of the previous tile has left TMEM
         if (it > 0 && !(ok = wait1(bars.dq_empty, (it - 1) & 1, wc, ERR_WAIT_MMA))) break;
         tc_fence_after();
@@ -284,12 +290,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         for (int kk = 0; kk < kT / 16; ++kk)
           mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8,
                  sdesc_sw128(do_a + kk * 2048, C::SUB, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q ; dQ = dS K
+        if (it + 1 < n) {
+          if (!(ok = wait1(&bars.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
+            break;
+          tc_fence_after();
+          issue_s(it + 1);
+        }
+        // dK += dS^T Q (A = dS^T: K-major view of the dS boxes) ; dQ = dS K
         if (!(ok = wait1(bars.ds_full, it & 1, wc, ERR_WAIT_MMA))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ts(t_dk, t_s + (kk / 4) * 64 + 32 + (kk % 4) * 8,
+          mma_ss(t_dk, sdesc_sw128(ds_a + (kk / 4) * C::SUB + (kk % 4) * 32, 16, 1024),
                  sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
@@ -318,7 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     constexpr int HD = D / 2;      // dQ / dK / dV columns per warpgroup
 
     // dQ of query tile `it` (TMEM lane = query row): read this warpgroup's
-    // columns, hand the TMEM region back, then reduce into the accumulator.
+    // columns, hand the TMEM region back, scale, and reduce-add them into the
+    // fp32 accumulator with TMA: each warp stages 32 rows x 32 columns at a
+    // time (a 128-byte-swizzled 4 KiB box) in its own slice of the dS buffer,
+    // which is free here (the dQ product that read it has completed) and
+    // which this warp rewrites with dS only after the reads below are done.
+    uint8_t* stage = ds_s + warp * 4096;
     auto dq_readout = [&](int it) -> bool {
       if (!wait_warp(bars.dq_full, it & 1, wc, ERR_WAIT_EPILOGUE)) return false;
       tc_fence_after();
@@ -328,91 +345,121 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(bars.dq_empty);
-      const int row = (i0 + it) * kT + r;
-      if (row < p.Nq) {
-        float* dst = a.dq_acc + ((size_t)bh * p.Nq + row) * D + h * HD;
+      const int row0 = (i0 + it) * kT + (warp % 4) * 32;
 #pragma unroll
-        for (int c = 0; c < HD; c += 4)
-          red_add_v4(dst + c, __uint_as_float(x[c]) * p.scale, __uint_as_float(x[c + 1]) * p.scale,
-                     __uint_as_float(x[c + 2]) * p.scale, __uint_as_float(x[c + 3]) * p.scale);
+      for (int c = 0; c < HD / 32; ++c) {
+        if (c > 0) {
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t* v = x + c * 32 + 4 * k;
+          *reinterpret_cast<uint4*>(stage + lane * 128 + ((k ^ (lane & 7)) * 16)) = make_uint4(
+              __float_as_uint(__uint_as_float(v[0]) * p.scale),
+              __float_as_uint(__uint_as_float(v[1]) * p.scale),
+              __float_as_uint(__uint_as_float(v[2]) * p.scale),
+              __float_as_uint(__uint_as_float(v[3]) * p.scale));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&a.tm_dqacc, stage, h * HD + c * 32, row0, bh);
+          bulk_commit_group();
+        }
       }
       return true;
     };
+    // lse2 (first 64 threads) or D (last 64) of one query row of tile `it`,
+    // loaded one iteration ahead so the load latency is hidden
+    auto stat_load = [&](int it) -> float {
+      const int row = (i0 + it) * kT + h * 64 + (r & 63);
+      const bool in = it < n && row < p.Nq;
+      if (r < 64) return in ? lse2g[(size_t)bh * p.Nq + row] : INFINITY;
+      return in ? Dg[(size_t)bh * p.Nq + row] : 0.f;
+    };
+    float stat_next = stat_load(0);
 
-    int it = 0;
-    bool ok = true;
-    for (; it < n; ++it) {
+    // P^T of query tile `it` = exp2(S^T * scale*log2e + bias - LSE2), masked
+    // -> 0, kept in fp32 registers for dS; packed bf16 copy to TMEM for dV.
+    float P[64];
+    auto compute_p = [&](int it) -> bool {
       const int q0 = (i0 + it) * kT;
-      if (it > 0 && !(ok = dq_readout(it - 1))) break;
-      // stage base-2 LSE (first 64) and D (last 64) of this warpgroup's query rows
-      float* st = stat + (h * 2 + (it & 1)) * kT;
-      {
-        const int row = q0 + h * 64 + (r & 63);
-        const bool in = row < p.Nq;
-        st[r] = r < 64 ? (in ? lse2g[(size_t)bh * p.Nq + row] : INFINITY)
-                       : (in ? Dg[(size_t)bh * p.Nq + row] : 0.f);
-      }
+      float* st = stat + (h * 2 + (it & 1)) * kT;   // staged base-2 LSE [0,64), D [64,128)
+      st[r] = stat_next;
+      stat_next = stat_load(it + 1);
       mbar_arrive(&bars.stat_rdy[h * 2 + (it & 1)]);
-      if (!(ok = wait_warp(&bars.stat_rdy[h * 2 + (it & 1)], (it >> 1) & 1, wc, ERR_WAIT_SOFTMAX)))
-        break;
-      if (!(ok = wait_warp(bars.s_full, it & 1, wc, ERR_WAIT_SOFTMAX))) break;
+      if (!wait_warp(&bars.stat_rdy[h * 2 + (it & 1)], (it >> 1) & 1, wc, ERR_WAIT_SOFTMAX))
+        return false;
+      if (!wait_warp(bars.s_full, it & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
-      // P^T = exp2(S^T * scale*log2e + bias - LSE2), masked -> 0; kept in fp32 for dS
       const bool need_mask = CAUSAL && ((long)q0 + off < (long)key0 + kT - 1);
       const long thr = (long)key - off - q0 - h * 64;   // local column < thr -> masked
-      float P[64];
+      uint32_t* sv = reinterpret_cast<uint32_t*>(P);
+      tmem_ld32(lane_base + h * 64, sv);
+      tmem_ld32(lane_base + h * 64 + 32, sv + 32);
+      tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(lane_base + h * 64 + c * 32, sv);
-        tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = fmaf(__uint_as_float(sv[e]), sl2, kb) - st[c * 32 + e];
-          if (need_mask && c * 32 + e < thr) x = -INFINITY;
-          P[c * 32 + e] = ex2(x);
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) pk[e / 2] = pack_bf16x2(P[c * 32 + e], P[c * 32 + e + 1]);
-        tmem_st16(lane_base + h * 64 + c * 16, pk);
+      for (int e = 0; e < 64; ++e) {
+        float x = fmaf(__uint_as_float(sv[e]), sl2, kb) - st[e];
+        if (need_mask && e < thr) x = -INFINITY;
+        P[e] = ex2(x);
       }
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) pk[e / 2] = pack_bf16x2(P[e], P[e + 1]);
+      tmem_st16(lane_base + h * 64, pk);
+      tmem_st16(lane_base + h * 64 + 16, pk + 16);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bars.p_full);
-
-      // dS^T = P^T o (dP^T - D), to TMEM (A of dK) and shared memory (A of dQ)
-      if (!(ok = wait_warp(bars.dp_full, it & 1, wc, ERR_WAIT_SOFTMAX))) break;
+      return true;
+    };
+    // dS^T = P^T o (dP^T - D) of query tile `it`, into the dS boxes in shared
+    // memory (A operand of dK += dS^T Q and of dQ = dS K).
+    auto compute_ds = [&](int it) -> bool {
+      const float* st = stat + (h * 2 + (it & 1)) * kT;
+      if (!wait_warp(bars.dp_full, it & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
+      uint32_t dpv[64];
+      tmem_ld32(lane_base + 128 + h * 64, dpv);
+      tmem_ld32(lane_base + 128 + h * 64 + 32, dpv + 32);
+      tmem_ld_wait();
+      uint32_t dsk[32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dpv[32];
-        tmem_ld32(lane_base + 128 + h * 64 + c * 32, dpv);
-        tmem_ld_wait();
-        uint32_t dsk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float d0 = P[c * 32 + e] * (__uint_as_float(dpv[e]) - st[64 + c * 32 + e]);
-          const float d1 =
-              P[c * 32 + e + 1] * (__uint_as_float(dpv[e + 1]) - st[64 + c * 32 + e + 1]);
-          dsk[e / 2] = pack_bf16x2(d0, d1);
-        }
-        tmem_st16(lane_base + h * 64 + 32 + c * 16, dsk);
-        // row = key of a 128-byte-swizzled box holding query columns [64h, 64h+64)
-        uint8_t* rowp = ds_s + h * C::SUB + r * 128;
-#pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          const int chunk = (c * 4 + v4) ^ (r & 7);
-          *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-              make_uint4(dsk[4 * v4], dsk[4 * v4 + 1], dsk[4 * v4 + 2], dsk[4 * v4 + 3]);
-        }
+      for (int e = 0; e < 64; e += 2) {
+        const float d0 = P[e] * (__uint_as_float(dpv[e]) - st[64 + e]);
+        const float d1 = P[e + 1] * (__uint_as_float(dpv[e + 1]) - st[64 + e + 1]);
+        dsk[e / 2] = pack_bf16x2(d0, d1);
       }
-      tmem_st_wait();
+      // the staged dQ of the previous tile must have been read by TMA
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+      // row = key of the 128-byte-swizzled box holding query columns [64h, 64h+64)
+      uint8_t* rowp = ds_s + h * C::SUB + r * 128;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int chunk = k ^ (r & 7);
+        *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+            make_uint4(dsk[4 * k], dsk[4 * k + 1], dsk[4 * k + 2], dsk[4 * k + 3]);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bars.ds_full);
+      return true;
+    };
+
+    // Order per tile i: dS(i), then P(i+1) (its S^T was issued right after
+    // dV(i)), then the read-out of dQ(i); P(0) first.
+    int it = 0;
+    bool ok = n == 0 || compute_p(0);
+    for (; ok && it < n; ++it) {
+      if (!(ok = compute_ds(it))) break;
+      if (it + 1 < n && !(ok = compute_p(it + 1))) break;
+      if (!(ok = dq_readout(it))) break;   // the last one: every MMA of this CTA is done
     }
-    if (ok && n > 0) ok = dq_readout(n - 1);   // also: every MMA of this CTA has completed
+    if (lane == 0) bulk_wait_group0();     // reductions complete before the CTA exits
+    __syncwarp();
     // ---- dK, dV of this key tile (this warpgroup's half of the columns)
     if (ok && it == n) {
       const bool have = n > 0;

@@ -87,6 +87,22 @@ fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D view (d, N, B*H) of the fp32 dQ accumulator for TMA reduce-add:
+// box (32, 32, 1) = one 128-byte-swizzled 4 KiB tile.
+fa_status make_map_f32_acc(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  EncodeTiledFn enc = nullptr;
+  fa_status st = get_encode(&enc);
+  if (st != FA_OK) return st;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -183,6 +199,8 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   a.D = reinterpret_cast<float*>(ws);
   a.lse2 = reinterpret_cast<float*>(ws + round256(rows * 4));
   a.dq_acc = reinterpret_cast<float*>(ws + 2 * round256(rows * 4));
+  if ((stages & fa::BWD_MAIN) && (st = make_map_f32_acc(&a.tm_dqacc, a.dq_acc, BH, Nq, d)) != FA_OK)
+    return st;
   a.dq = static_cast<uint16_t*>(dq);
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);

@@ -32,11 +32,13 @@ struct FwdBf16Args {
   uint16_t* o;         // bf16 [B][H][Nq][d]
   float* lse;
   uint32_t* err;       // device error word
+  int head_group;      // heads per CTA-ordering group (set by the launcher)
 };
 
 struct BwdBf16Args {
   Problem p;
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_dqacc;   // fp32 dQ accumulator as (d, Nq, B*H), box (32, 32, 1), 128B swizzle
   const uint16_t* o;
   const uint16_t* dO;
   const float* lse;

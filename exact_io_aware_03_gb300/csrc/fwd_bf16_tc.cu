@@ -40,6 +40,7 @@
 //    (they contribute exactly zero);
 //  - a row with no visible key keeps m = -inf and l = 0 and is written as
 //    O = 0, LSE = -inf.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -124,11 +125,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   float* bias_buf = reinterpret_cast<float*>(smem + C::OFF_BIAS);
   const WaitCtx wc{abort_flag, a.err};
 
-  // ---- which (query-tile pair, head): heaviest causal tiles first
-  const int BH = p.B * p.H;
+  // ---- which (query-tile pair, head). Heads are taken in groups of
+  // a.head_group whose K/V fit comfortably in L2; within a group the CTAs go
+  // heaviest first (last query tiles, the most key tiles under a causal mask),
+  // cycling over the group's heads, so that both L2 reuse of K/V and the load
+  // balance of the causal triangle are kept.
   const int n_pairs = (p.Nq + 2 * kBM - 1) / (2 * kBM);
-  const int pair = n_pairs - 1 - (int)(blockIdx.x / BH);
-  const int bh = (int)(blockIdx.x % BH);
+  const int BH = p.B * p.H;
+  const int G = a.head_group;
+  const int grp = (int)(blockIdx.x / (G * n_pairs));
+  const int g0 = grp * G;
+  const int gsz = min(G, BH - g0);
+  const int rr = (int)(blockIdx.x - (long)g0 * n_pairs);
+  const int bh = g0 + rr % gsz;
+  const int pair = n_pairs - 1 - rr / gsz;
   const int b = bh / p.H;
   const int q_base = pair * 2 * kBM;
   const float* bias_row = BIAS ? a.bias + (size_t)b * p.Nk : nullptr;
@@ -356,7 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
 
       const bool need_mask = (long)key0 + kBN - 1 > lim_tile;
       const bool scaled = BIAS || need_mask;
-      float mx = -INFINITY;
+      // row max as 8 independent partial maxima (no serial dependency chain)
+      float m8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
       if (scaled) {
         const float* bb = bias_buf + (t * 2 + (i & 1)) * kBN;
         const long lim_rel = lim_row - key0;
@@ -365,13 +378,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
           float v = BIAS ? fmaf(s[c], sl2, bb[c]) : s[c] * sl2;
           if (need_mask && c > lim_rel) v = -INFINITY;
           s[c] = v;
-          mx = fmaxf(mx, v);
+          m8[c & 7] = fmaxf(m8[c & 7], v);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, s[c]);
-        mx *= sl2;
+        for (int c = 0; c < kBN; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
       }
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      if (!scaled) mx *= sl2;
       // conditional move of the running max
       float alpha = 1.f;
       bool moved = false;
@@ -381,7 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         m = mx;
       }
       const float mu = (m == -INFINITY) ? 0.f : m;
-      float psum = 0.f;
+      float ps[8];   // row sum as 8 independent partial sums
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ps[k] = 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < kBN; c0 += 32) {
         uint32_t pk[16];
@@ -389,11 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         for (int c = 0; c < 32; c += 2) {
           const float p0 = scaled ? ex2(s[c0 + c] - mu) : ex2(fmaf(s[c0 + c], sl2, -mu));
           const float p1 = scaled ? ex2(s[c0 + c + 1] - mu) : ex2(fmaf(s[c0 + c + 1], sl2, -mu));
-          psum += p0 + p1;
+          ps[(c / 2) & 7] += p0 + p1;
           pk[c / 2] = pack_bf16x2(p0, p1);
         }
         tmem_st16(lane_base + s_col + c0 / 2, pk);
       }
+      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l = l * alpha + psum;
       // rescale O if any row of this warp moved its max and O already holds data
       if (__any_sync(0xffffffffu, moved) && i > 0) {
@@ -468,7 +486,11 @@ cudaError_t launch_one(const FwdBf16Args& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const long BH = (long)a.p.B * a.p.H;
   const long n_pairs = (a.p.Nq + 2 * kBM - 1) / (2 * kBM);
-  kern<<<(unsigned)(BH * n_pairs), kThreads, C::SMEM_ALLOC, s>>>(a);
+  // heads per ordering group: K and V of a group within ~48 MiB of L2
+  const long kv_bytes = 2L * a.p.Nk * D * 2;
+  FwdBf16Args b = a;
+  b.head_group = (int)std::max(1L, std::min(BH, (48L << 20) / std::max(kv_bytes, 1L)));
+  kern<<<(unsigned)(BH * n_pairs), kThreads, C::SMEM_ALLOC, s>>>(b);
   return cudaGetLastError();
 }
 

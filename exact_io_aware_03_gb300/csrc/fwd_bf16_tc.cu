@@ -366,26 +366,30 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
 
       const bool need_mask = (long)key0 + kBN - 1 > lim_tile;
       const bool scaled = BIAS || need_mask;
-      // row max as 8 independent partial maxima (no serial dependency chain)
-      float m8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+      // Scores are handled in pairs with the packed f32x2 instructions, and
+      // the row max with the three-input max: about three instructions per
+      // score in total.
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (scaled) {
         const float* bb = bias_buf + (t * 2 + (i & 1)) * kBN;
         const long lim_rel = lim_row - key0;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          float v = BIAS ? fmaf(s[c], sl2, bb[c]) : s[c] * sl2;
-          if (need_mask && c > lim_rel) v = -INFINITY;
-          s[c] = v;
-          m8[c & 7] = fmaxf(m8[c & 7], v);
+        for (int c = 0; c < kBN; c += 2) {
+          const uint64_t b2 = BIAS ? *reinterpret_cast<const uint64_t*>(bb + c) : 0ull;
+          float v0, v1;
+          f2_unpack(fma2(f2_pack(s[c], s[c + 1]), sl2x2, b2), v0, v1);
+          if (need_mask && c > lim_rel) v0 = -INFINITY;
+          if (need_mask && c + 1 > lim_rel) v1 = -INFINITY;
+          s[c] = v0;
+          s[c + 1] = v1;
+          m4[(c / 2) & 3] = fmax3(m4[(c / 2) & 3], v0, v1);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+        for (int c = 0; c < kBN; c += 2) m4[(c / 2) & 3] = fmax3(m4[(c / 2) & 3], s[c], s[c + 1]);
       }
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       if (!scaled) mx *= sl2;
       // conditional move of the running max
       float alpha = 1.f;
@@ -396,21 +400,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         m = mx;
       }
       const float mu = (m == -INFINITY) ? 0.f : m;
-      float ps[8];   // row sum as 8 independent partial sums
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+      // p = exp2(s * scale*log2e - mu) (or exp2(s - mu) for scores already in
+      // the base-2 domain), as one packed FMA per pair
+      const uint64_t mul2 = scaled ? f2_pack(1.f, 1.f) : f2_pack(sl2, sl2);
+      const uint64_t nmu2 = f2_pack(-mu, -mu);
+      uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};   // row sum as 4 packed partial sums
 #pragma unroll
       for (int c0 = 0; c0 < kBN; c0 += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const float p0 = scaled ? ex2(s[c0 + c] - mu) : ex2(fmaf(s[c0 + c], sl2, -mu));
-          const float p1 = scaled ? ex2(s[c0 + c + 1] - mu) : ex2(fmaf(s[c0 + c + 1], sl2, -mu));
-          ps[(c / 2) & 7] += p0 + p1;
+          float x0, x1;
+          f2_unpack(fma2(f2_pack(s[c0 + c], s[c0 + c + 1]), mul2, nmu2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          ps2[(c / 2) & 3] = add2(ps2[(c / 2) & 3], f2_pack(p0, p1));
           pk[c / 2] = pack_bf16x2(p0, p1);
         }
         tmem_st16(lane_base + s_col + c0 / 2, pk);
       }
+      float ps[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) f2_unpack(ps2[k], ps[2 * k], ps[2 * k + 1]);
       const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l = l * alpha + psum;
       // rescale O if any row of this warp moved its max and O already holds data

@@ -52,17 +52,27 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
                                                       const float* __restrict__ lse,
                                                       float* __restrict__ Dv,
                                                       float* __restrict__ lse2,
-                                                      float* __restrict__ dq_acc, long rows) {
+                                                      float* __restrict__ dq_acc, long BH,
+                                                      int Nq, int nq_pad) {
+  // Statistics are laid out per head with nq_pad (a multiple of 128) rows, so
+  // that every 128-row tile of them is one aligned 512-byte block; the padding
+  // rows get D = 0 and base-2 LSE = +inf (their recomputed P is exactly 0).
   constexpr int LPR = D / 8;          // lanes per row, 8 bf16 (16 B) per lane
   constexpr int RPW = 32 / LPR;       // rows per warp step
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, li = lane % LPR;
   const long warp_g = ((long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const long nwarps = ((long)gridDim.x * blockDim.x) / 32;
-  for (long r0 = warp_g * RPW; r0 < rows; r0 += nwarps * RPW) {
-    const long row = r0 + sub;
+  const long prows = BH * nq_pad;
+  for (long r0 = warp_g * RPW; r0 < prows; r0 += nwarps * RPW) {
+    const long pr = r0 + sub;            // padded row index
+    const bool in = pr < prows;
+    const long bh = pr / nq_pad;
+    const int i = (int)(pr - bh * nq_pad);
+    const bool valid = in && i < Nq;
+    const long row = bh * Nq + i;        // row of O, dO, LSE and the dQ accumulator
     float acc = 0.f;
-    if (row < rows) {
+    if (valid) {
       const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[li];
       const uint4 g = reinterpret_cast<const uint4*>(dO + row * D)[li];
       const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
@@ -78,10 +88,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
     }
 #pragma unroll
     for (int w = LPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-    if (row < rows && li == 0) {
-      Dv[row] = acc;
-      const float L = lse[row];
-      lse2[row] = (L == -INFINITY) ? INFINITY : L * kLog2e;
+    if (in && li == 0) {
+      Dv[pr] = valid ? acc : 0.f;
+      const float L = valid ? lse[row] : -INFINITY;
+      lse2[pr] = (L == -INFINITY) ? INFINITY : L * kLog2e;
     }
   }
 }
@@ -105,27 +115,29 @@ struct BwdCfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
   static constexpr int OFF_Q = OFF_V + TILE;         // [2 stages]
-  static constexpr int OFF_DO = OFF_Q + 2 * TILE;    // [2 stages]
-  static constexpr int OFF_DS = OFF_DO + 2 * TILE;
-  // [2 warpgroups][2 bufs] {lse2[64], D[64]}
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;    // [1 stage]
+  static constexpr int OFF_DQST = OFF_DO + TILE;     // 32 KiB: second dQ staging slice
+  static constexpr int OFF_DS = OFF_DQST + 32768;
+  // per Q stage: base-2 LSE [128] then D [128] of the tile's rows (TMA)
   static constexpr int OFF_STAT = OFF_DS + DS_BYTES;
   static constexpr int OFF_BAR = OFF_STAT + 2 * 2 * kT * 4;
-  static constexpr int NBAR = 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 4 + 1;
+  static constexpr int NBAR = 1 + 2 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 1;
   static constexpr int OFF_SCALARS = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_SCALARS + 32;
 };
 
 struct BwdBars {
   uint64_t* kv_full;   // [1]
-  uint64_t* q_full;    // [2]  Q_i and dO_i of a stage
+  uint64_t* q_full;    // [2]  Q_i and its base-2 LSE and D of a stage
   uint64_t* q_empty;   // [2]
+  uint64_t* do_full;   // dO_i (single buffer)
+  uint64_t* do_empty;
   uint64_t* s_full;    // S^T done
   uint64_t* dp_full;   // dP^T done
   uint64_t* p_full;    // P^T in TMEM (128 arrivals)
   uint64_t* ds_full;   // dS^T in TMEM + smem (128 arrivals)
   uint64_t* dq_full;   // dQ_i done (and everything before it)
   uint64_t* dq_empty;  // dQ_i read out of TMEM (128 arrivals)
-  uint64_t* stat_rdy;  // [2 warpgroups][2 bufs] lse2/D staged (128 arrivals)
   uint64_t* drain;
 };
 
@@ -143,13 +155,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   bars.kv_full = bb; bb += 1;
   bars.q_full = bb; bb += 2;
   bars.q_empty = bb; bb += 2;
+  bars.do_full = bb; bb += 1;
+  bars.do_empty = bb; bb += 1;
   bars.s_full = bb; bb += 1;
   bars.dp_full = bb; bb += 1;
   bars.p_full = bb; bb += 1;
   bars.ds_full = bb; bb += 1;
   bars.dq_full = bb; bb += 1;
   bars.dq_empty = bb; bb += 1;
-  bars.stat_rdy = bb; bb += 4;
   bars.drain = bb;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_SCALARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SCALARS + 4);
@@ -183,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
     }
-    for (int s = 0; s < 4; ++s) mbar_init(&bars.stat_rdy[s], kT);
+    mbar_init(bars.do_full, 1);
+    mbar_init(bars.do_empty, 1);
     mbar_init(bars.s_full, 1);
     mbar_init(bars.dp_full, 1);
     mbar_init(bars.p_full, 2 * kT);
@@ -221,24 +235,32 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, key0, bh, bars.kv_full);
         tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, key0, bh, bars.kv_full);
       }
-      int issued = 0;
+      int nq = 0, nd = 0;   // Q / dO fills issued
       for (int it = 0; it < n; ++it) {
         const int s = it & 1, u = it >> 1;
-        if (u > 0 && !wait1(&bars.q_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
         const int q0 = (i0 + it) * kT;
-        mbar_arrive_expect_tx(&bars.q_full[s], 2 * C::TILE);
-        for (int c = 0; c < D / 64; ++c) {
+        if (u > 0 && !wait1(&bars.q_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
+        mbar_arrive_expect_tx(&bars.q_full[s], C::TILE + 2 * kT * 4);
+        for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * C::SUB, &a.tm_q, c * 64, q0, bh,
                       &bars.q_full[s]);
-          tma_load_3d(smem + C::OFF_DO + s * C::TILE + c * C::SUB, &a.tm_do, c * 64, q0, bh,
-                      &bars.q_full[s]);
-        }
-        ++issued;
+        float* st = reinterpret_cast<float*>(smem + C::OFF_STAT) + s * 2 * kT;
+        const size_t srow = (size_t)bh * a.nq_pad + q0;
+        bulk_load_1d(st, a.lse2 + srow, kT * 4, &bars.q_full[s]);
+        bulk_load_1d(st + kT, a.D + srow, kT * 4, &bars.q_full[s]);
+        ++nq;
+        // dO has one buffer: its next tile may land once dV of this one is done
+        if (it > 0 && !wait1(bars.do_empty, (it - 1) & 1, wc, ERR_WAIT_LOAD)) break;
+        mbar_arrive_expect_tx(bars.do_full, C::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::OFF_DO + c * C::SUB, &a.tm_do, c * 64, q0, bh, bars.do_full);
+        ++nd;
       }
       const WaitCtx wd{abort_flag, a.err, true};
       wait1(bars.kv_full, 0, wd, ERR_WAIT_DRAIN);
-      for (int it = max(0, issued - 2); it < issued; ++it)
+      for (int it = max(0, nq - 2); it < nq; ++it)
         wait1(&bars.q_full[it & 1], (it >> 1) & 1, wd, ERR_WAIT_DRAIN);
+      if (nd > 0) wait1(bars.do_full, (nd - 1) & 1, wd, ERR_WAIT_DRAIN);
     }
   } else if (warp == 9) {
     // ================================================================ MMA issuer
@@ -271,9 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       for (int it = 0; it < n && ok; ++it) {
         const int s = it & 1;
         const uint32_t q_a = smem_u32(smem + C::OFF_Q + s * C::TILE);
-        const uint32_t do_a = smem_u32(smem + C::OFF_DO + s * C::TILE);
+        const uint32_t do_a = smem_u32(smem + C::OFF_DO);
         // dP^T = V dO^T, once dQ of the previous tile has left TMEM
         if (it > 0 && !(ok = wait1(bars.dq_empty, (it - 1) & 1, wc, ERR_WAIT_MMA))) break;
+        if (!(ok = wait1(bars.do_full, it & 1, wc, ERR_WAIT_MMA))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -290,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         for (int kk = 0; kk < kT / 16; ++kk)
           mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8,
                  sdesc_sw128(do_a + kk * 2048, C::SUB, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bars.do_empty);   // dV is the last reader of dO(it)
         if (it + 1 < n) {
           if (!(ok = wait1(&bars.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
             break;
@@ -323,19 +347,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     const int key = key0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const float sl2 = p.scale * kLog2e;
-    const float* lse2g = a.lse;    // base-2 LSE (workspace copy written by bwd_pre)
-    const float* Dg = a.D;
     float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);
     uint8_t* ds_s = smem + C::OFF_DS;
     constexpr int HD = D / 2;      // dQ / dK / dV columns per warpgroup
 
     // dQ of query tile `it` (TMEM lane = query row): read this warpgroup's
     // columns, hand the TMEM region back, scale, and reduce-add them into the
-    // fp32 accumulator with TMA: each warp stages 32 rows x 32 columns at a
-    // time (a 128-byte-swizzled 4 KiB box) in its own slice of the dS buffer,
-    // which is free here (the dQ product that read it has completed) and
-    // which this warp rewrites with dS only after the reads below are done.
-    uint8_t* stage = ds_s + warp * 4096;
+    // fp32 accumulator with TMA: each warp stages its 32 rows as 128-byte-
+    // swizzled boxes of 32 columns (4 KiB each) in its own slice of the dS
+    // buffer (free here: the dQ product that read it has completed) and of a
+    // second staging area; it rewrites them only after TMA has read them.
+    // chunk 0 in this warp's slice of the dS boxes, chunk 1 in its slice of
+    // the second staging area
+    uint8_t* stage0 = ds_s + warp * 4096;
+    uint8_t* stage1 = smem + C::OFF_DQST + warp * 4096;
     auto dq_readout = [&](int it) -> bool {
       if (!wait_warp(bars.dq_full, it & 1, wc, ERR_WAIT_EPILOGUE)) return false;
       tc_fence_after();
@@ -348,10 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       const int row0 = (i0 + it) * kT + (warp % 4) * 32;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
-        if (c > 0) {
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
-        }
+        uint8_t* stage = c == 0 ? stage0 : stage1;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t* v = x + c * 32 + 4 * k;
@@ -361,36 +383,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
               __float_as_uint(__uint_as_float(v[2]) * p.scale),
               __float_as_uint(__uint_as_float(v[3]) * p.scale));
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_3d(&a.tm_dqacc, stage, h * HD + c * 32, row0, bh);
-          bulk_commit_group();
-        }
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c)
+          tma_reduce_add_3d(&a.tm_dqacc, c == 0 ? stage0 : stage1, h * HD + c * 32, row0, bh);
+      }
+      if (lane == 0) bulk_commit_group();
       return true;
     };
-    // lse2 (first 64 threads) or D (last 64) of one query row of tile `it`,
-    // loaded one iteration ahead so the load latency is hidden
-    auto stat_load = [&](int it) -> float {
-      const int row = (i0 + it) * kT + h * 64 + (r & 63);
-      const bool in = it < n && row < p.Nq;
-      if (r < 64) return in ? lse2g[(size_t)bh * p.Nq + row] : INFINITY;
-      return in ? Dg[(size_t)bh * p.Nq + row] : 0.f;
-    };
-    float stat_next = stat_load(0);
-
     // P^T of query tile `it` = exp2(S^T * scale*log2e + bias - LSE2), masked
     // -> 0, kept in fp32 registers for dS; packed bf16 copy to TMEM for dV.
     float P[64];
     auto compute_p = [&](int it) -> bool {
       const int q0 = (i0 + it) * kT;
-      float* st = stat + (h * 2 + (it & 1)) * kT;   // staged base-2 LSE [0,64), D [64,128)
-      st[r] = stat_next;
-      stat_next = stat_load(it + 1);
-      mbar_arrive(&bars.stat_rdy[h * 2 + (it & 1)]);
-      if (!wait_warp(&bars.stat_rdy[h * 2 + (it & 1)], (it >> 1) & 1, wc, ERR_WAIT_SOFTMAX))
-        return false;
+      // this tile's base-2 LSE (staged by TMA with Q) for this warpgroup's columns
+      if (!wait_warp(&bars.q_full[it & 1], (it >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) return false;
+      const float* stl = stat + (it & 1) * 2 * kT + h * 64;
       if (!wait_warp(bars.s_full, it & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
       const bool need_mask = CAUSAL && ((long)q0 + off < (long)key0 + kT - 1);
@@ -399,11 +410,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tmem_ld32(lane_base + h * 64, sv);
       tmem_ld32(lane_base + h * 64 + 32, sv + 32);
       tmem_ld_wait();
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), kb2 = f2_pack(kb, kb);
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        float x = fmaf(__uint_as_float(sv[e]), sl2, kb) - st[e];
-        if (need_mask && e < thr) x = -INFINITY;
-        P[e] = ex2(x);
+      for (int e = 0; e < 64; e += 4) {
+        const float4 L4 = *reinterpret_cast<const float4*>(stl + e);
+        float x[4];
+        f2_unpack(sub2(fma2(f2_pack(P[e], P[e + 1]), sl2x2, kb2), f2_pack(L4.x, L4.y)), x[0], x[1]);
+        f2_unpack(sub2(fma2(f2_pack(P[e + 2], P[e + 3]), sl2x2, kb2), f2_pack(L4.z, L4.w)), x[2],
+                  x[3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (need_mask && e + j < thr) x[j] = -INFINITY;
+          P[e + j] = ex2(x[j]);
+        }
       }
       uint32_t pk[32];
 #pragma unroll
@@ -418,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // dS^T = P^T o (dP^T - D) of query tile `it`, into the dS boxes in shared
     // memory (A operand of dK += dS^T Q and of dQ = dS K).
     auto compute_ds = [&](int it) -> bool {
-      const float* st = stat + (h * 2 + (it & 1)) * kT;
+      const float* std_ = stat + (it & 1) * 2 * kT + kT + h * 64;
       if (!wait_warp(bars.dp_full, it & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
       uint32_t dpv[64];
@@ -427,10 +446,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tmem_ld_wait();
       uint32_t dsk[32];
 #pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        const float d0 = P[e] * (__uint_as_float(dpv[e]) - st[64 + e]);
-        const float d1 = P[e + 1] * (__uint_as_float(dpv[e + 1]) - st[64 + e + 1]);
-        dsk[e / 2] = pack_bf16x2(d0, d1);
+      for (int e = 0; e < 64; e += 4) {
+        const float4 D4 = *reinterpret_cast<const float4*>(std_ + e);
+        float d[4];
+        f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                            f2_pack(D4.x, D4.y)),
+                       f2_pack(P[e], P[e + 1])),
+                  d[0], d[1]);
+        f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
+                            f2_pack(D4.z, D4.w)),
+                       f2_pack(P[e + 2], P[e + 3])),
+                  d[2], d[3]);
+        dsk[e / 2] = pack_bf16x2(d[0], d[1]);
+        dsk[e / 2 + 1] = pack_bf16x2(d[2], d[3]);
       }
       // the staged dQ of the previous tile must have been read by TMA
       if (lane == 0) bulk_wait_group_read0();
@@ -520,14 +548,15 @@ cudaError_t launch_d(const BwdBf16Args& a, cudaStream_t s, unsigned stages) {
   cudaError_t e = cudaSuccess;
   if (stages & BWD_PRE) {
     constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
-    const long blocks = min((rows + kRowsPerBlock - 1) / kRowsPerBlock, (long)a.num_sms * 8);
+    const long BH = (long)a.p.B * a.p.H;
+    const long prows = BH * a.nq_pad;
+    const long blocks = min((prows + kRowsPerBlock - 1) / kRowsPerBlock, (long)a.num_sms * 8);
     bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a.o, a.dO, a.lse, a.D, a.lse2, a.dq_acc,
-                                                      rows);
+                                                      BH, a.p.Nq, a.nq_pad);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (stages & BWD_MAIN) {
-    BwdBf16Args m = a;
-    m.lse = a.lse2;   // the main kernel reads the base-2 LSE written by the preprocess
+    const BwdBf16Args& m = a;
     const bool bias = a.bias != nullptr;
     if (a.p.causal)
       e = bias ? launch_main<D, true, true>(m, s) : launch_main<D, true, false>(m, s);

@@ -155,7 +155,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, const float* key_b
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
   const size_t rows = (size_t)B * H * Nq;
-  return 2 * round256(rows * 4) + round256(rows * (size_t)d * 4);
+  const size_t prow = (size_t)B * H * (((size_t)Nq + 127) / 128 * 128);   // 128-row padded
+  return 2 * round256(prow * 4) + round256(rows * (size_t)d * 4);
 }
 
 }  // extern "C"
@@ -194,11 +195,12 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   a.dO = static_cast<const uint16_t*>(dO);
   a.lse = lse;
   a.bias = key_bias;
-  const size_t rows = (size_t)BH * Nq;
+  a.nq_pad = (Nq + 127) / 128 * 128;
+  const size_t prow = (size_t)BH * a.nq_pad;
   char* ws = static_cast<char*>(workspace);
   a.D = reinterpret_cast<float*>(ws);
-  a.lse2 = reinterpret_cast<float*>(ws + round256(rows * 4));
-  a.dq_acc = reinterpret_cast<float*>(ws + 2 * round256(rows * 4));
+  a.lse2 = reinterpret_cast<float*>(ws + round256(prow * 4));
+  a.dq_acc = reinterpret_cast<float*>(ws + 2 * round256(prow * 4));
   if ((stages & fa::BWD_MAIN) && (st = make_map_f32_acc(&a.tm_dqacc, a.dq_acc, BH, Nq, d)) != FA_OK)
     return st;
   a.dq = static_cast<uint16_t*>(dq);

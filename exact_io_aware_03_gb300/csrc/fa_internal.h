@@ -43,14 +43,16 @@ struct BwdBf16Args {
   const uint16_t* dO;
   const float* lse;
   const float* bias;
-  float* D;            // workspace: rowsum(dO o O), [B][H][Nq]
-  float* lse2;         // workspace: LSE * log2(e) (+inf for fully masked rows)
+  float* D;            // workspace: rowsum(dO o O), [B*H][nq_pad] (0 in the padding)
+  float* lse2;         // workspace: LSE * log2(e), [B*H][nq_pad] (+inf for fully
+                       // masked rows and in the padding)
   float* dq_acc;       // workspace: fp32 dQ accumulator [B][H][Nq][d]
   uint16_t* dq;
   uint16_t* dk;
   uint16_t* dv;
   uint32_t* err;
   int num_sms;
+  int nq_pad;          // Nq rounded up to a multiple of 128
 };
 
 cudaError_t launch_fwd_f32(const FwdF32Args& a, cudaStream_t s);

@@ -82,9 +82,9 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, const float *key_b
                  fa_dtype dtype, void *stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: D = rowsum(dO o O) as fp32
- * [B,H,Nq], the LSE rescaled to base 2 as fp32 [B,H,Nq], and an fp32 dQ
- * accumulator [B,H,Nq,d], each starting on a 256-byte boundary.
+ * Bytes of device workspace fa_bwd needs: D = rowsum(dO o O) and the LSE
+ * rescaled to base 2, each fp32 [B*H][Nq rounded up to a multiple of 128],
+ * and an fp32 dQ accumulator [B,H,Nq,d], each starting on a 256-byte boundary.
  * Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d);

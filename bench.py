@@ -230,6 +230,27 @@ def run_reference(args):
 
 # --------------------------------------------------------------------------- GPU arm
 
+def replica_seed(w, rank):
+    """Each replica draws its own batch: the workload's seed offset by the rank."""
+    return w.seed + rank
+
+
+def replica_throughput(ms_total_local, steps, flops_per_step, world, device=None):
+    """Whole-job throughput of `world` independent replicas.
+
+    The timed region of each rank is `ms_total_local` milliseconds for `steps`
+    steps of `flops_per_step` FLOPs; the job time is the slowest rank's (MAX
+    over ranks), and the job's work is every rank's. Returns (ms per step,
+    TFLOP/s). With world > 1 this is a collective: every rank must call it.
+    """
+    import torch
+    t = torch.tensor([float(ms_total_local)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step = float(t.item()) / steps
+    return ms_step, flops_per_step * world / (ms_step * 1e-3) / 1e12
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -252,7 +273,7 @@ def run_ours(args):
 
     w = workloads.WORKLOADS[WORKLOAD]
     f_fwd, f_bwd = flops(w)
-    x = workloads.make_inputs(w, with_dO=True, seed=w.seed + rank)
+    x = workloads.make_inputs(w, with_dO=True, seed=replica_seed(w, rank))
     q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
@@ -301,12 +322,7 @@ def run_ours(args):
     ms_total = t_start.elapsed_time(t_end)
     parts = {n: [e[j].elapsed_time(e[j + 1]) for e in evs]
              for j, n in enumerate(["fwd", "bwd_preprocess", "bwd_main", "bwd_postprocess"])}
-    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total = float(t.item())
-    ms_step = ms_total / args.steps
-    value = (f_fwd + f_bwd) * world / (ms_step * 1e-3) / 1e12
+    ms_step, value = replica_throughput(ms_total, args.steps, f_fwd + f_bwd, world, dev)
 
     # ---- end to end through the public API: pinned host inputs in, results out
     e2e_steps = max(3, min(args.steps, 20))
@@ -341,10 +357,7 @@ def run_ours(args):
     a1.record(stream)
     torch.cuda.synchronize(dev)
     fa.check_device_error(dev)
-    te = torch.tensor([a0.elapsed_time(a1) / e2e_steps], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = (f_fwd + f_bwd) * world / (float(te.item()) * 1e-3) / 1e12
+    _, e2e_value = replica_throughput(a0.elapsed_time(a1), e2e_steps, f_fwd + f_bwd, world, dev)
 
     # ---- extra forward-only measurement on the long-context causal workload
     extras = {}

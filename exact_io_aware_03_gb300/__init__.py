@@ -55,6 +55,8 @@ def load(path=None):
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_get_last_device_error.argtypes = [vp]
     lib.fa_get_last_device_error.restype = cint
+    lib.fa_selftest_device_timeout.argtypes = [vp]
+    lib.fa_selftest_device_timeout.restype = cint
     _lib = lib
     return lib
 
@@ -100,6 +102,10 @@ def fa_status_string(status):
 
 def fa_get_last_device_error(stream):
     return load().fa_get_last_device_error(stream)
+
+
+def fa_selftest_device_timeout(stream):
+    return load().fa_selftest_device_timeout(stream)
 
 
 FA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024

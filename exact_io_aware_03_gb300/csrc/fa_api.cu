@@ -12,6 +12,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace {
 
@@ -104,6 +105,20 @@ fa_status make_map_f32_acc(CUtensorMap* m, const void* base, int BH, int N, int 
 }
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// One thread waits (bounded) on an mbarrier that nothing ever arrives at, so
+// the wait runs out: it records FA_ERR_DEVICE's code in the error word and
+// returns, exactly as a stalled pipeline stage in the real kernels would.
+__global__ void selftest_timeout_kernel(uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  fa::mbar_init(&bar, 1);
+  abort_flag = 0;
+  fa::fence_mbar_init();
+  const fa::WaitCtx w{&abort_flag, err};
+  fa::wait1(&bar, 0, w, fa::ERR_WAIT_SOFTMAX);
+}
 
 }  // namespace
 
@@ -255,6 +270,14 @@ fa_status fa_bwd_postprocess(const void* q, const void* k, const void* v, const 
 }
 
 #undef FA_BWD_ARGS
+
+fa_status fa_selftest_device_timeout(void* stream) {
+  uint32_t* err = nullptr;
+  fa_status st = get_err_ptr(&err);
+  if (st != FA_OK) return st;
+  selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 fa_status fa_get_last_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;

@@ -178,6 +178,16 @@ const char *fa_status_string(fa_status s);
  */
 fa_status fa_get_last_device_error(void *stream);
 
+/*
+ * Diagnostic of the device-side failure path: launches one thread that waits,
+ * with the same bounded wait the kernels use, on a barrier nothing arrives at.
+ * After about 2 seconds the wait gives up, records a timeout in the device
+ * error word and the kernel returns, leaving the context usable; the next
+ * fa_get_last_device_error returns FA_ERR_DEVICE (and clears the word).
+ * Returns FA_ERR_CUDA if the launch fails.
+ */
+fa_status fa_selftest_device_timeout(void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,6 +33,7 @@ import workloads  # noqa: E402
 
 WORKLOAD = "bf16_b4h16_n4096_d128_causal_bwd"
 FWD_EXTRA = "bf16_b2h32_n8192_d128_causal"
+DECODE_EXTRA = "bf16_b8h32_q1_k32768_d128_decode"
 METRIC = "attention fwd/bwd TFLOP/s (bf16, causal, d=128) and % of GB300 tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
@@ -382,6 +383,32 @@ def run_ours(args):
         extras[FWD_EXTRA + "_fwd_tflops"] = flops(we)[0] / (ms_e * 1e-3) / 1e12
         extras[FWD_EXTRA + "_fwd_ms"] = ms_e
         del qe, ke, ve, oe, le
+        # decode step through the split-KV forward: HBM-bound (K and V read once)
+        wd = workloads.WORKLOADS[DECODE_EXTRA]
+        qd, kd, vd = (torch.randn((wd.B, wd.H, n, wd.d), generator=g, device=dev,
+                                  dtype=torch.bfloat16) for n in (wd.Nq, wd.Nk, wd.Nk))
+        with torch.cuda.device(dev):
+            ns = fa.fa_fwd_splitkv_default_splits(wd.B, wd.H, wd.Nq, wd.Nk, wd.d)
+        wsd = torch.empty(fa.fa_fwd_splitkv_workspace_size(wd.B, wd.H, wd.Nq, wd.Nk, wd.d, ns),
+                          dtype=torch.uint8, device=dev)
+        od = torch.empty_like(qd)
+        ld = torch.empty(qd.shape[:3], dtype=torch.float32, device=dev)
+        for _ in range(3):
+            fa.fwd_splitkv(qd, kd, vd, num_splits=ns, out=od, lse=ld, workspace=wsd)
+        b0.record(stream)
+        for _ in range(n_e):
+            fa.fwd_splitkv(qd, kd, vd, num_splits=ns, out=od, lse=ld, workspace=wsd)
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        fa.check_device_error(dev)
+        ms_d = b0.elapsed_time(b1) / n_e
+        kv_bytes = 2.0 * wd.B * wd.H * wd.Nk * wd.d * 2
+        extras[DECODE_EXTRA + "_splits"] = ns
+        extras[DECODE_EXTRA + "_ms"] = ms_d
+        extras[DECODE_EXTRA + "_kv_gbs"] = kv_bytes / (ms_d * 1e-3) / 1e9
+        extras[DECODE_EXTRA + "_kv_frac_of_hbm"] = (kv_bytes / (ms_d * 1e-3) / 1e9
+                                                    / load_peaks()[0].get("hbm_gbs", 6800.0))
+        del qd, kd, vd, od, ld, wsd
 
     if rank != 0:
         if world > 1:

@@ -46,6 +46,13 @@ def load(path=None):
     lib.fa_fwd.restype = cint
     lib.fa_bwd_workspace_size.argtypes = [cint] * 5
     lib.fa_bwd_workspace_size.restype = csz
+    lib.fa_fwd_splitkv_workspace_size.argtypes = [cint] * 6
+    lib.fa_fwd_splitkv_workspace_size.restype = csz
+    lib.fa_fwd_splitkv_default_splits.argtypes = [cint] * 5
+    lib.fa_fwd_splitkv_default_splits.restype = cint
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint, cf, cint,
+                                   cint, vp, csz, vp]
+    lib.fa_fwd_splitkv.restype = cint
     for name in ("fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess"):
         f = getattr(lib, name)
         f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint,
@@ -66,6 +73,20 @@ def load(path=None):
 def fa_fwd(q, k, v, key_bias, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, stream):
     return load().fa_fwd(q, k, v, key_bias, o, lse, B, H, Nq, Nk, d, scale, causal, dtype,
                          stream)
+
+
+def fa_fwd_splitkv(q, k, v, key_bias, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits,
+                   workspace, workspace_bytes, stream):
+    return load().fa_fwd_splitkv(q, k, v, key_bias, o, lse, B, H, Nq, Nk, d, scale, causal,
+                                 num_splits, workspace, workspace_bytes, stream)
+
+
+def fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits):
+    return load().fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits)
+
+
+def fa_fwd_splitkv_default_splits(B, H, Nq, Nk, d):
+    return load().fa_fwd_splitkv_default_splits(B, H, Nq, Nk, d)
 
 
 def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale, causal, dtype,
@@ -175,6 +196,36 @@ def fwd(q, k, v, key_bias=None, causal=False, scale=None, out=None, lse=None):
                     _stream(q))
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
+    return out, lse
+
+
+def fwd_splitkv(q, k, v, key_bias=None, causal=False, scale=None, num_splits=None, out=None,
+                lse=None, workspace=None):
+    """Split-KV forward (bf16): same results as ``fwd``; num_splits=None picks a
+    split count that fills the device."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    if num_splits is None:
+        with torch.cuda.device(q.device):
+            num_splits = fa_fwd_splitkv_default_splits(B, H, Nq, Nk, d)
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(1, fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d,
+                                                                     num_splits)),
+                                dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(key_bias), _ptr(out), _ptr(lse),
+                            B, H, Nq, Nk, d, float(scale), int(bool(causal)), int(num_splits),
+                            _ptr(workspace), workspace.numel(), _stream(q))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_splitkv")
     return out, lse
 
 

@@ -4,6 +4,7 @@
 // variable) whose address is looked up once per device.
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -120,6 +121,23 @@ __global__ void selftest_timeout_kernel(uint32_t* err) {
   fa::wait1(&bar, 0, w, fa::ERR_WAIT_SOFTMAX);
 }
 
+// Tensor maps and pointers of the bf16 forward (everything but the split).
+fa_status fwd_bf16_setup(fa::FwdBf16Args* a, const fa::Problem& p, const void* q, const void* k,
+                         const void* v, const float* key_bias, void* o, float* lse) {
+  std::memset(a, 0, sizeof(*a));
+  a->p = p;
+  const int BH = p.B * p.H;
+  fa_status st;
+  if ((st = make_map(&a->tm_q, q, BH, p.Nq, p.d)) != FA_OK) return st;
+  if ((st = make_map(&a->tm_k, k, BH, p.Nk, p.d)) != FA_OK) return st;
+  if ((st = make_map(&a->tm_v, v, BH, p.Nk, p.d)) != FA_OK) return st;
+  a->bias = key_bias;
+  a->o = static_cast<uint16_t*>(o);
+  a->lse = lse;
+  a->n_split = 1;
+  return get_err_ptr(&a->err);
+}
+
 }  // namespace
 
 extern "C" {
@@ -154,17 +172,56 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, const float* key_b
   }
   if (!lse) return FA_ERR_INVALID_ARG;
   fa::FwdBf16Args a;
-  std::memset(&a, 0, sizeof(a));
-  a.p = p;
-  const int BH = B * H;
-  if ((st = make_map(&a.tm_q, q, BH, Nq, d)) != FA_OK) return st;
-  if ((st = make_map(&a.tm_k, k, BH, Nk, d)) != FA_OK) return st;
-  if ((st = make_map(&a.tm_v, v, BH, Nk, d)) != FA_OK) return st;
-  a.bias = key_bias;
-  a.o = static_cast<uint16_t*>(o);
-  a.lse = lse;
-  if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
+  st = fwd_bf16_setup(&a, p, q, k, v, key_bias, o, lse);
+  if (st != FA_OK) return st;
   return fa::launch_fwd_bf16(a, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || num_splits < 1) return 0;
+  const size_t rows = (size_t)num_splits * B * H * Nq;
+  return round256(rows * (size_t)d * 4) + round256(rows * 4);
+}
+
+int fa_fwd_splitkv_default_splits(int B, int H, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  const long ctas = (long)B * H * ((Nq + 255) / 256);
+  const long n_kv = (Nk + 127) / 128;
+  // enough CTAs for two waves, each split keeping at least 4 key tiles
+  long splits = (2L * sms + ctas - 1) / ctas;
+  splits = std::min(splits, std::max(1L, n_kv / 4));
+  return (int)std::max(1L, std::min(splits, 128L));
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, const float* key_bias,
+                         void* o, float* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                         int causal, int num_splits, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  fa_status st = check_problem(B, H, Nq, Nk, d, scale, FA_DTYPE_BF16);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(workspace, 256) || !aligned(lse, 4) || (key_bias && !aligned(key_bias, 4)))
+    return FA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > 1024) return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits))
+    return FA_ERR_INVALID_ARG;
+  fa::Problem p{B, H, Nq, Nk, d, scale, causal ? 1 : 0};
+  fa::FwdBf16Args a;
+  st = fwd_bf16_setup(&a, p, q, k, v, key_bias, o, lse);
+  if (st != FA_OK) return st;
+  if (num_splits > 1) {
+    const size_t rows = (size_t)num_splits * B * H * Nq;
+    a.n_split = num_splits;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * d * 4));
+  }
+  return fa::launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                   : FA_ERR_CUDA;
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d) {

@@ -33,6 +33,9 @@ struct FwdBf16Args {
   float* lse;
   uint32_t* err;       // device error word
   int head_group;      // heads per CTA-ordering group (set by the launcher)
+  int n_split;         // split-KV: number of key ranges (1 = off)
+  float* part_o;       // split-KV workspace: fp32 O [n_split][B*H][Nq][d]
+  float* part_lse;     // split-KV workspace: LSE [n_split][B*H][Nq]
 };
 
 struct BwdBf16Args {

@@ -219,6 +219,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     }
     hi_t[t] = max(h, lo);
   }
+  if (a.n_split > 1) {
+    // split-KV: this CTA covers key tiles [s_lo, s_hi) of its query tiles only
+    const int per = (n_kv + a.n_split - 1) / a.n_split;
+    const int s_lo = (int)blockIdx.y * per, s_hi = min(n_kv, s_lo + per);
+    lo = max(lo, s_lo);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) hi_t[t] = max(lo, min(hi_t[t], s_hi));
+  }
   const int hi = max(hi_t[0], hi_t[1]);
   const bool any = hi > lo;
 
@@ -448,7 +456,33 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       if (!wait_warp(&bars.o_done[t], (n_t - 1) & 1, wc, ERR_WAIT_SOFTMAX)) have_o = false;
       tc_fence_after();
     }
-    if (completed) {
+    if (completed && a.n_split > 1) {
+      // partial result of this key range: normalised O in fp32 and its LSE,
+      // merged by the combine kernel
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t prow = ((size_t)blockIdx.y * p.B * p.H + bh) * p.Nq + row_g;
+      float* orow = a.part_o + prow * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        if (have_o) {
+          tmem_ld32(lane_base + o_col + c0, ov);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = 0u;
+        }
+        if (row_g < p.Nq) {
+          float4* dst = reinterpret_cast<float4*>(orow + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            dst[v4] = make_float4(__uint_as_float(ov[4 * v4]) * inv, __uint_as_float(ov[4 * v4 + 1]) * inv,
+                                  __uint_as_float(ov[4 * v4 + 2]) * inv,
+                                  __uint_as_float(ov[4 * v4 + 3]) * inv);
+        }
+      }
+      if (row_g < p.Nq) a.part_lse[prow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    } else if (completed) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint16_t* orow = a.o + ((size_t)bh * p.Nq + row_g) * D;
 #pragma unroll
@@ -487,6 +521,47 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   }
 }
 
+// Split-KV combine (the merge of partial softmax states over disjoint key
+// ranges: "flash-attention", Part VI; "FlashAttention: Mathematical
+// Foundations...", Flash-Decoding): with partial (O_s, LSE_s),
+//   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s.
+// One warp per query row; a row whose every partial is empty stays O = 0,
+// LSE = -inf.
+template <int D>
+__global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __restrict__ part_o,
+                                                              const float* __restrict__ part_lse,
+                                                              uint16_t* __restrict__ o,
+                                                              float* __restrict__ lse, long rows,
+                                                              int n_split) {
+  const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < n_split; ++s) mx = fmaxf(mx, part_lse[(long)s * rows + row]);
+  constexpr int PER = D / 32;   // columns per lane
+  float acc[PER];
+#pragma unroll
+  for (int c = 0; c < PER; ++c) acc[c] = 0.f;
+  float sum = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < n_split; ++s) {
+      const float ls = part_lse[(long)s * rows + row];
+      if (ls == -INFINITY) continue;
+      const float w = __expf(ls - mx);
+      sum += w;
+      const float* src = part_o + ((long)s * rows + row) * D + lane * PER;
+#pragma unroll
+      for (int c = 0; c < PER; ++c) acc[c] = fmaf(w, src[c], acc[c]);
+    }
+  }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  uint16_t* dst = o + row * D + lane * PER;
+#pragma unroll
+  for (int c = 0; c < PER; c += 2)
+    *reinterpret_cast<uint32_t*>(dst + c) = pack_bf16x2(acc[c] * inv, acc[c + 1] * inv);
+  if (lane == 0) lse[row] = sum > 0.f ? mx + __logf(sum) : -INFINITY;
+}
+
 template <int D, bool CAUSAL, bool BIAS>
 cudaError_t launch_one(const FwdBf16Args& a, cudaStream_t s) {
   using C = FwdCfg<D>;
@@ -500,7 +575,13 @@ cudaError_t launch_one(const FwdBf16Args& a, cudaStream_t s) {
   const long kv_bytes = 2L * a.p.Nk * D * 2;
   FwdBf16Args b = a;
   b.head_group = (int)std::max(1L, std::min(BH, (48L << 20) / std::max(kv_bytes, 1L)));
-  kern<<<(unsigned)(BH * n_pairs), kThreads, C::SMEM_ALLOC, s>>>(b);
+  const dim3 grid((unsigned)(BH * n_pairs), (unsigned)std::max(1, a.n_split));
+  kern<<<grid, kThreads, C::SMEM_ALLOC, s>>>(b);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.n_split <= 1) return e;
+  const long rows = BH * a.p.Nq;
+  splitkv_combine_kernel<D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, s>>>(
+      a.part_o, a.part_lse, a.o, a.lse, rows, a.n_split);
   return cudaGetLastError();
 }
 

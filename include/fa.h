@@ -82,6 +82,27 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, const float *key_b
                  fa_dtype dtype, void *stream);
 
 /*
+ * Split-KV forward (Flash-Decoding) for problems with few query rows and many
+ * keys, e.g. decoding: the keys of every (b, h) are cut into num_splits
+ * contiguous ranges processed by separate CTAs, each producing a partial
+ * normalised output O_s (fp32) and its log-sum-exp LSE_s in the workspace;
+ * a second launch merges them with the log-sum-exp rule
+ *   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
+ * ("flash-attention", Part VI; "FlashAttention: Mathematical Foundations...",
+ * Flash-Decoding). Same arguments, layout and results as fa_fwd (bf16 only),
+ * plus num_splits >= 1 (1 = no split, no workspace use) and a device
+ * workspace of fa_fwd_splitkv_workspace_size(...) bytes, 256-byte aligned.
+ * fa_fwd_splitkv_default_splits gives a split count that fills the device
+ * (uses the current device's SM count; no launch).
+ */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+int fa_fwd_splitkv_default_splits(int B, int H, int Nq, int Nk, int d);
+fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, const float *key_bias,
+                         void *o, float *lse,
+                         int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                         int num_splits, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: D = rowsum(dO o O) and the LSE
  * rescaled to base 2, each fp32 [B*H][Nq rounded up to a multiple of 128],
  * and an fp32 dQ accumulator [B,H,Nq,d], each starting on a 256-byte boundary.

@@ -118,3 +118,21 @@ def test_binding_refuses_to_run_without_the_library(tmp_path):
             mod.load(str(tmp_path / "missing.so"))
     finally:
         mod._lib = saved
+
+
+def test_splitkv_workspace_and_validation(lib):
+    B, H, Nq, Nk, d, S = 2, 3, 5, 1000, 128, 4
+    rows = S * B * H * Nq
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert fa.fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, S) == r256(rows * d * 4) + r256(rows * 4)
+    assert fa.fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, 0) == 0
+    assert fa.fa_fwd_splitkv_default_splits(B, H, Nq, Nk, d) >= 1
+    a = dict(q=FAKE, k=FAKE, v=FAKE, key_bias=None, o=FAKE, lse=FAKE, B=B, H=H, Nq=Nq, Nk=Nk,
+             d=d, scale=0.1, causal=0, num_splits=S, workspace=FAKE, workspace_bytes=1 << 30,
+             stream=None)
+    for bad in (dict(num_splits=0), dict(workspace=None), dict(workspace_bytes=16),
+                dict(workspace=FAKE + 64), dict(lse=None), dict(d=80)):
+        b = dict(a)
+        b.update(bad)
+        st = fa.fa_fwd_splitkv(**b)
+        assert st in (fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED), bad

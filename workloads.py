@@ -12,8 +12,9 @@ Recipe (same for every consumer):
   * key-padding problems: the valid key length of batch b is a uniform integer
     in [Nk/2, Nk] (inclusive); bias[b, j] = 0 for j < L_b and -inf otherwise.
 
-The named workloads below are the five problem shapes the benchmark and the
-parity tests run; their seeds are 1001..1005.
+The named workloads below are the problem shapes the benchmark and the parity
+tests run; their seeds are 1001..1006 (the sixth, a decode step, exercises the
+split-KV forward).
 """
 from __future__ import annotations
 
@@ -67,6 +68,10 @@ WORKLOADS = {
     "bf16_b8h16_q1024_k16384_d128_keypad": Workload("bf16_b8h16_q1024_k16384_d128_keypad", 8, 16,
                                                     1024, 16384, 128, "bf16", False, True, True,
                                                     1005),
+    # decode step with a long key/value context: one query row per head
+    # (the split-KV forward's workload)
+    "bf16_b8h32_q1_k32768_d128_decode": Workload("bf16_b8h32_q1_k32768_d128_decode", 8, 32, 1,
+                                                 32768, 128, "bf16", False, False, False, 1006),
 }
 
 

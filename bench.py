@@ -409,6 +409,30 @@ def run_ours(args):
         extras[DECODE_EXTRA + "_kv_frac_of_hbm"] = (kv_bytes / (ms_d * 1e-3) / 1e9
                                                     / load_peaks()[0].get("hbm_gbs", 6800.0))
         del qd, kd, vd, od, ld, wsd
+        # grouped-query attention: the step's workload with 4 key/value heads
+        hk = 4
+        qg, dOg = (torch.randn((w.B, w.H, w.Nq, w.d), generator=g, device=dev,
+                               dtype=torch.bfloat16) for _ in range(2))
+        kg, vg = (torch.randn((w.B, hk, w.Nk, w.d), generator=g, device=dev,
+                              dtype=torch.bfloat16) for _ in range(2))
+        og = torch.empty_like(qg)
+        lg = torch.empty(qg.shape[:3], dtype=torch.float32, device=dev)
+        dqg, dkg, dvg = torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)
+
+        def gqa_step():
+            fa.fwd(qg, kg, vg, out=og, lse=lg, **kw)
+            fa.bwd(qg, kg, vg, og, lg, dOg, workspace=ws, dq=dqg, dk=dkg, dv=dvg, **kw)
+        for _ in range(3):
+            gqa_step()
+        b0.record(stream)
+        for _ in range(n_e):
+            gqa_step()
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        fa.check_device_error(dev)
+        ms_g = b0.elapsed_time(b1) / n_e
+        extras["gqa_b4h16kv4_n4096_d128_causal_fwdbwd_tflops"] = (f_fwd + f_bwd) / (ms_g * 1e-3) / 1e12
+        del qg, dOg, kg, vg, og, lg, dqg, dkg, dvg
 
     if rank != 0:
         if world > 1:

@@ -50,8 +50,14 @@ def load(path=None):
     lib.fa_fwd_splitkv_workspace_size.restype = csz
     lib.fa_fwd_splitkv_default_splits.argtypes = [cint] * 5
     lib.fa_fwd_splitkv_default_splits.restype = cint
-    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint, cf, cint,
-                                   cint, vp, csz, vp]
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint, cint, cf,
+                                   cint, cint, vp, csz, vp]
+    lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint, cint, cf,
+                               cint, cint, vp]
+    lib.fa_fwd_gqa.restype = cint
+    lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, cint, cint, cint, cint,
+                               cint, cint, cf, cint, cint, vp, csz, vp]
+    lib.fa_bwd_gqa.restype = cint
     lib.fa_fwd_splitkv.restype = cint
     for name in ("fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess"):
         f = getattr(lib, name)
@@ -75,10 +81,21 @@ def fa_fwd(q, k, v, key_bias, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, str
                          stream)
 
 
-def fa_fwd_splitkv(q, k, v, key_bias, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits,
+def fa_fwd_splitkv(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal, num_splits,
                    workspace, workspace_bytes, stream):
-    return load().fa_fwd_splitkv(q, k, v, key_bias, o, lse, B, H, Nq, Nk, d, scale, causal,
+    return load().fa_fwd_splitkv(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal,
                                  num_splits, workspace, workspace_bytes, stream)
+
+
+def fa_fwd_gqa(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal, dtype, stream):
+    return load().fa_fwd_gqa(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal,
+                             dtype, stream)
+
+
+def fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d, scale, causal,
+               dtype, workspace, workspace_bytes, stream):
+    return load().fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d,
+                             scale, causal, dtype, workspace, workspace_bytes, stream)
 
 
 def fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits):
@@ -183,7 +200,7 @@ def fwd(q, k, v, key_bias=None, causal=False, scale=None, out=None, lse=None):
     if key_bias is not None:
         _check(key_bias, "key_bias")
     B, H, Nq, d = q.shape
-    Nk = k.shape[2]
+    Hkv, Nk = k.shape[1], k.shape[2]
     if scale is None:
         scale = d ** -0.5
     if out is None:
@@ -191,11 +208,11 @@ def fwd(q, k, v, key_bias=None, causal=False, scale=None, out=None, lse=None):
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
-        st = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(key_bias), _ptr(out), _ptr(lse),
-                    B, H, Nq, Nk, d, float(scale), int(bool(causal)), _dtype_code(q),
-                    _stream(q))
+        st = fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(key_bias), _ptr(out), _ptr(lse),
+                        B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)), _dtype_code(q),
+                        _stream(q))
     if st != FA_OK:
-        raise FaError(st, "fa_fwd")
+        raise FaError(st, "fa_fwd_gqa")
     return out, lse
 
 
@@ -207,7 +224,7 @@ def fwd_splitkv(q, k, v, key_bias=None, causal=False, scale=None, num_splits=Non
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, n)
     B, H, Nq, d = q.shape
-    Nk = k.shape[2]
+    Hkv, Nk = k.shape[1], k.shape[2]
     if scale is None:
         scale = d ** -0.5
     if num_splits is None:
@@ -222,7 +239,7 @@ def fwd_splitkv(q, k, v, key_bias=None, causal=False, scale=None, num_splits=Non
                                 dtype=torch.uint8, device=q.device)
     with torch.cuda.device(q.device):
         st = fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(key_bias), _ptr(out), _ptr(lse),
-                            B, H, Nq, Nk, d, float(scale), int(bool(causal)), int(num_splits),
+                            B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)), int(num_splits),
                             _ptr(workspace), workspace.numel(), _stream(q))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_splitkv")
@@ -240,7 +257,7 @@ def bwd(q, k, v, o, lse, dO, key_bias=None, causal=False, scale=None, workspace=
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (dO, "dO")):
         _check(t, n)
     B, H, Nq, d = q.shape
-    Nk = k.shape[2]
+    Hkv, Nk = k.shape[1], k.shape[2]
     if scale is None:
         scale = d ** -0.5
     dq = torch.empty_like(q) if dq is None else dq
@@ -249,13 +266,20 @@ def bwd(q, k, v, o, lse, dO, key_bias=None, causal=False, scale=None, workspace=
     ws_bytes = fa_bwd_workspace_size(B, H, Nq, Nk, d)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    fn = {None: fa_bwd, "preprocess": fa_bwd_preprocess, "main": fa_bwd_main,
-          "postprocess": fa_bwd_postprocess}[stage]
+    if stage is None:
+        fn = fa_bwd_gqa
+        heads = (B, H, Hkv)
+    else:
+        if Hkv != H:
+            raise ValueError("the single-stage backward calls take H_kv == H")
+        fn = {"preprocess": fa_bwd_preprocess, "main": fa_bwd_main,
+              "postprocess": fa_bwd_postprocess}[stage]
+        heads = (B, H)
     with torch.cuda.device(q.device):
         st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
-                    _ptr(dk), _ptr(dv), _ptr(key_bias), B, H, Nq, Nk, d, float(scale),
-                    int(bool(causal)), _dtype_code(q), _ptr(workspace), workspace.numel(),
-                    _stream(q))
+                _ptr(dk), _ptr(dv), _ptr(key_bias), *heads, Nq, Nk, d, float(scale),
+                int(bool(causal)), _dtype_code(q), _ptr(workspace), workspace.numel(),
+                _stream(q))
     if st != FA_OK:
         raise FaError(st, fn.__name__)
     return dq, dk, dv

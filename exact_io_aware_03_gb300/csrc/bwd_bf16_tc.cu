@@ -172,10 +172,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   // Head-major order: the CTAs running together cover few heads, so their Q,
   // dO and dQ accumulator stay in L2; within a head the low key tiles (the
   // most query tiles under a causal mask) come first.
+  // One CTA per (key/value head, key tile). With grouped heads it walks the
+  // query tiles of every query head of its group, so dK and dV of the shared
+  // head accumulate over the whole group in TMEM.
   const int n_kt = (p.Nk + kT - 1) / kT;
-  const int bh = (int)(blockIdx.x / n_kt);
+  const int bh_kv = (int)(blockIdx.x / n_kt);
   const int jt = (int)(blockIdx.x % n_kt);
-  const int b = bh / p.H;
+  const int b = bh_kv / p.Hkv;
+  const int grp = p.H / p.Hkv;
+  const int bh_q0 = b * p.H + (bh_kv % p.Hkv) * grp;   // first query head of the group
   const int key0 = jt * kT;
   const long off = (long)p.Nk - p.Nq;
 
@@ -188,6 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     i0 = need <= 0 ? 0 : (int)min((long)n_qt, (need + kT - 1) / kT);
   }
   const int i1 = n_qt;
+  const int nqh = i1 - i0;   // query tiles per query head
+  // query head and tile of step `it` of this CTA
+  auto q_head = [&](int it) { return bh_q0 + it / max(nqh, 1); };
+  auto q_row0 = [&](int it) { return (i0 + it % max(nqh, 1)) * kT; };
 
   if (threadIdx.x == 0) {
     if ((smem_u32(smem) & 1023u) != 0) atomicOr(a.err, ERR_WAIT_DRAIN);   // layout invariant
@@ -225,20 +234,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n = (*any_key && !*abort_flag) ? max(0, i1 - i0) : 0;
+  const int n = (*any_key && !*abort_flag) ? max(0, nqh) * grp : 0;
 
   if (warp == 8) {
     // ================================================================ TMA producer
     if (lane == 0 && n > 0) {
       mbar_arrive_expect_tx(bars.kv_full, 2 * C::TILE);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, key0, bh, bars.kv_full);
-        tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, key0, bh, bars.kv_full);
+        tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, key0, bh_kv, bars.kv_full);
+        tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, key0, bh_kv, bars.kv_full);
       }
       int nq = 0, nd = 0;   // Q / dO fills issued
       for (int it = 0; it < n; ++it) {
         const int s = it & 1, u = it >> 1;
-        const int q0 = (i0 + it) * kT;
+        const int q0 = q_row0(it), bh = q_head(it);
         if (u > 0 && !wait1(&bars.q_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
         mbar_arrive_expect_tx(&bars.q_full[s], C::TILE + 2 * kT * 4);
         for (int c = 0; c < D / 64; ++c)
@@ -370,7 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(bars.dq_empty);
-      const int row0 = (i0 + it) * kT + (warp % 4) * 32;
+      const int row0 = q_row0(it) + (warp % 4) * 32;
+      const int bh = q_head(it);
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint8_t* stage = c == 0 ? stage0 : stage1;
@@ -398,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // -> 0, kept in fp32 registers for dS; packed bf16 copy to TMEM for dV.
     float P[64];
     auto compute_p = [&](int it) -> bool {
-      const int q0 = (i0 + it) * kT;
+      const int q0 = q_row0(it);
       // this tile's base-2 LSE (staged by TMA with Q) for this warpgroup's columns
       if (!wait_warp(&bars.q_full[it & 1], (it >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       const float* stl = stat + (it & 1) * 2 * kT + h * 64;
@@ -491,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // ---- dK, dV of this key tile (this warpgroup's half of the columns)
     if (ok && it == n) {
       const bool have = n > 0;
-      const size_t base = ((size_t)bh * p.Nk + key) * D + h * HD;
+      const size_t base = ((size_t)bh_kv * p.Nk + key) * D + h * HD;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {   // 0: dV, 1: dK
         uint16_t* dst = (which ? a.dk : a.dv) + base;
@@ -536,9 +546,9 @@ cudaError_t launch_main(const BwdBf16Args& a, cudaStream_t s) {
   auto kern = bwd_main_kernel<D, CAUSAL, BIAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
   if (e != cudaSuccess) return e;
-  const long BH = (long)a.p.B * a.p.H;
+  const long BHkv = (long)a.p.B * a.p.Hkv;
   const long n_kt = (a.p.Nk + kT - 1) / kT;
-  kern<<<(unsigned)(BH * n_kt), kThreads, C::BYTES, s>>>(a);
+  kern<<<(unsigned)(BHkv * n_kt), kThreads, C::BYTES, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -59,8 +59,10 @@ fa_status get_err_ptr(uint32_t** out) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Shared size/shape checks. Returns FA_OK or the error.
-fa_status check_problem(int B, int H, int Nq, int Nk, int d, float scale, fa_dtype dtype) {
+fa_status check_problem(int B, int H, int Nq, int Nk, int d, float scale, fa_dtype dtype,
+                        int Hkv) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
@@ -129,8 +131,8 @@ fa_status fwd_bf16_setup(fa::FwdBf16Args* a, const fa::Problem& p, const void* q
   const int BH = p.B * p.H;
   fa_status st;
   if ((st = make_map(&a->tm_q, q, BH, p.Nq, p.d)) != FA_OK) return st;
-  if ((st = make_map(&a->tm_k, k, BH, p.Nk, p.d)) != FA_OK) return st;
-  if ((st = make_map(&a->tm_v, v, BH, p.Nk, p.d)) != FA_OK) return st;
+  if ((st = make_map(&a->tm_k, k, p.B * p.Hkv, p.Nk, p.d)) != FA_OK) return st;
+  if ((st = make_map(&a->tm_v, v, p.B * p.Hkv, p.Nk, p.d)) != FA_OK) return st;
   a->bias = key_bias;
   a->o = static_cast<uint16_t*>(o);
   a->lse = lse;
@@ -156,14 +158,20 @@ const char* fa_status_string(fa_status s) {
 fa_status fa_fwd(const void* q, const void* k, const void* v, const float* key_bias, void* o,
                  float* lse, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                  fa_dtype dtype, void* stream) {
-  fa_status st = check_problem(B, H, Nq, Nk, d, scale, dtype);
+  return fa_fwd_gqa(q, k, v, key_bias, o, lse, B, H, H, Nq, Nk, d, scale, causal, dtype, stream);
+}
+
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, const float* key_bias, void* o,
+                     float* lse, int B, int H, int H_kv, int Nq, int Nk, int d, float scale,
+                     int causal, fa_dtype dtype, void* stream) {
+  fa_status st = check_problem(B, H, Nq, Nk, d, scale, dtype, H_kv);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
     return FA_ERR_INVALID_ARG;
   if ((key_bias && !aligned(key_bias, 4)) || (lse && !aligned(lse, 4))) return FA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  fa::Problem p{B, H, Nq, Nk, d, scale, causal ? 1 : 0};
+  fa::Problem p{B, H, Nq, Nk, d, scale, causal ? 1 : 0, H_kv};
 
   if (dtype == FA_DTYPE_FP32) {
     fa::FwdF32Args a{p, static_cast<const float*>(q), static_cast<const float*>(k),
@@ -198,10 +206,10 @@ int fa_fwd_splitkv_default_splits(int B, int H, int Nq, int Nk, int d) {
 }
 
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, const float* key_bias,
-                         void* o, float* lse, int B, int H, int Nq, int Nk, int d, float scale,
-                         int causal, int num_splits, void* workspace, size_t workspace_bytes,
-                         void* stream) {
-  fa_status st = check_problem(B, H, Nq, Nk, d, scale, FA_DTYPE_BF16);
+                         void* o, float* lse, int B, int H, int H_kv, int Nq, int Nk, int d,
+                         float scale, int causal, int num_splits, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  fa_status st = check_problem(B, H, Nq, Nk, d, scale, FA_DTYPE_BF16, H_kv);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
@@ -210,7 +218,7 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, const floa
   if (num_splits < 1 || num_splits > 1024) return FA_ERR_INVALID_ARG;
   if (workspace_bytes < fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits))
     return FA_ERR_INVALID_ARG;
-  fa::Problem p{B, H, Nq, Nk, d, scale, causal ? 1 : 0};
+  fa::Problem p{B, H, Nq, Nk, d, scale, causal ? 1 : 0, H_kv};
   fa::FwdBf16Args a;
   st = fwd_bf16_setup(&a, p, q, k, v, key_bias, o, lse);
   if (st != FA_OK) return st;
@@ -238,10 +246,10 @@ namespace {
 // Validation and argument set-up shared by fa_bwd and its three stages.
 fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                     const float* key_bias, int B, int H, int Nq, int Nk, int d, float scale,
-                     int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
-                     void* stream, unsigned stages) {
-  fa_status st = check_problem(B, H, Nq, Nk, d, scale, dtype);
+                     const float* key_bias, int B, int H, int Hkv, int Nq, int Nk, int d,
+                     float scale, int causal, fa_dtype dtype, void* workspace,
+                     size_t workspace_bytes, void* stream, unsigned stages) {
+  fa_status st = check_problem(B, H, Nq, Nk, d, scale, dtype, Hkv);
   if (st != FA_OK) return st;
   if (dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
@@ -255,12 +263,12 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
 
   fa::BwdBf16Args a;
   std::memset(&a, 0, sizeof(a));
-  a.p = fa::Problem{B, H, Nq, Nk, d, scale, causal ? 1 : 0};
+  a.p = fa::Problem{B, H, Nq, Nk, d, scale, causal ? 1 : 0, Hkv};
   const int BH = B * H;
   if (stages & fa::BWD_MAIN) {
     if ((st = make_map(&a.tm_q, q, BH, Nq, d)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_k, k, BH, Nk, d)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_v, v, BH, Nk, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_k, k, B * Hkv, Nk, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_v, v, B * Hkv, Nk, d)) != FA_OK) return st;
     if ((st = make_map(&a.tm_do, dO, BH, Nq, d)) != FA_OK) return st;
   }
   a.o = static_cast<const uint16_t*>(o);
@@ -291,8 +299,8 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
 
 extern "C" {
 
-#define FA_BWD_ARGS                                                                        \
-  q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, Nq, Nk, d, scale, causal, dtype, workspace, \
+#define FA_BWD_ARGS                                                                          \
+  q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H, Nq, Nk, d, scale, causal, dtype, workspace, \
       workspace_bytes, stream
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -327,6 +335,16 @@ fa_status fa_bwd_postprocess(const void* q, const void* k, const void* v, const 
 }
 
 #undef FA_BWD_ARGS
+
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                     const float* key_bias, int B, int H, int H_kv, int Nq, int Nk, int d,
+                     float scale, int causal, fa_dtype dtype, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d, scale,
+                    causal, dtype, workspace, workspace_bytes, stream,
+                    fa::BWD_PRE | fa::BWD_MAIN | fa::BWD_POST);
+}
 
 fa_status fa_selftest_device_timeout(void* stream) {
   uint32_t* err = nullptr;

@@ -6,11 +6,14 @@
 
 namespace fa {
 
-// Problem description shared by all kernels. Tensors are [B][H][N][d].
+// Problem description shared by all kernels. q, o, dO, dq are [B][H][Nq][d];
+// k, v, dk, dv are [B][Hkv][Nk][d] with H a multiple of Hkv: query head h
+// attends key/value head h / (H / Hkv) (Hkv == H: plain multi-head).
 struct Problem {
   int B, H, Nq, Nk, d;
   float scale;   // multiplies Q K^T
   int causal;    // bottom-right causal mask when non-zero
+  int Hkv;       // key/value heads
 };
 
 struct FwdF32Args {

@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   const int bh = g0 + rr % gsz;
   const int pair = n_pairs - 1 - rr / gsz;
   const int b = bh / p.H;
+  const int bh_kv = b * p.Hkv + (bh % p.H) / (p.H / p.Hkv);   // key/value head of this query head
   const int q_base = pair * 2 * kBM;
   const float* bias_row = BIAS ? a.bias + (size_t)b * p.Nk : nullptr;
 
@@ -247,13 +248,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         if (u > 0 && !wait1(&bars.k_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
         mbar_arrive_expect_tx(&bars.k_full[s], C::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::SUB, &a.tm_k, c * 64, j * kBN, bh,
+          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::SUB, &a.tm_k, c * 64, j * kBN, bh_kv,
                       &bars.k_full[s]);
         ++nk;
         if (u > 0 && !wait1(&bars.v_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
         mbar_arrive_expect_tx(&bars.v_full[s], C::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::SUB, &a.tm_v, c * 64, j * kBN, bh,
+          tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::SUB, &a.tm_v, c * 64, j * kBN, bh_kv,
                       &bars.v_full[s]);
         ++nv;
       }

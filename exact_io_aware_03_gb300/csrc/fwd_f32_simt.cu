@@ -42,8 +42,9 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(FwdF32Args a) {
   const bool row_ok = row < p.Nq;
 
   const float* qh = a.q + (size_t)bh * p.Nq * D;
-  const float* kh = a.k + (size_t)bh * p.Nk * D;
-  const float* vh = a.v + (size_t)bh * p.Nk * D;
+  const long bh_kv = (long)b * p.Hkv + (bh % p.H) / (p.H / p.Hkv);   // shared key/value head
+  const float* kh = a.k + (size_t)bh_kv * p.Nk * D;
+  const float* vh = a.v + (size_t)bh_kv * p.Nk * D;
   const float* bias = a.bias ? a.bias + (size_t)b * p.Nk : nullptr;
 
   const float sl2 = p.scale * kLog2e;

@@ -82,6 +82,26 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, const float *key_b
                  fa_dtype dtype, void *stream);
 
 /*
+ * Grouped-query / multi-query attention ("Understanding FlashAttention Pt 1",
+ * Part 4.1; "flash-attention", the MQA/GQA note): q, o (and dO, dq) are
+ * [B,H,N,d]; k, v (and dk, dv) are [B,H_kv,Nk,d] with H a multiple of H_kv;
+ * query head h attends key/value head h / (H / H_kv). H_kv == H is plain
+ * multi-head attention (fa_fwd / fa_bwd are these calls with H_kv = H);
+ * H_kv == 1 is multi-query attention. dk and dv of a shared head sum the
+ * contributions of every query head of its group. Otherwise identical to
+ * fa_fwd / fa_bwd (same workspace size, as a function of B, H, Nq, Nk, d).
+ */
+fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, const float *key_bias,
+                     void *o, float *lse,
+                     int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int causal,
+                     fa_dtype dtype, void *stream);
+fa_status fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
+                     const float *lse, const void *dO,
+                     void *dq, void *dk, void *dv, const float *key_bias,
+                     int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int causal,
+                     fa_dtype dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Split-KV forward (Flash-Decoding) for problems with few query rows and many
  * keys, e.g. decoding: the keys of every (b, h) are cut into num_splits
  * contiguous ranges processed by separate CTAs, each producing a partial
@@ -89,7 +109,7 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, const float *key_b
  * a second launch merges them with the log-sum-exp rule
  *   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
  * ("flash-attention", Part VI; "FlashAttention: Mathematical Foundations...",
- * Flash-Decoding). Same arguments, layout and results as fa_fwd (bf16 only),
+ * Flash-Decoding). Same arguments, layout and results as fa_fwd_gqa (bf16 only),
  * plus num_splits >= 1 (1 = no split, no workspace use) and a device
  * workspace of fa_fwd_splitkv_workspace_size(...) bytes, 256-byte aligned.
  * fa_fwd_splitkv_default_splits gives a split count that fills the device
@@ -99,7 +119,7 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int nu
 int fa_fwd_splitkv_default_splits(int B, int H, int Nq, int Nk, int d);
 fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, const float *key_bias,
                          void *o, float *lse,
-                         int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                         int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int causal,
                          int num_splits, void *workspace, size_t workspace_bytes, void *stream);
 
 /*

@@ -247,3 +247,28 @@ def fwd_head_rows(qh, kh, vh, bias_row, rows, scale, causal):
                              _ptr(o), _ptr(lse), Nq, Nk, d, float(scale), int(bool(causal)),
                              _ptr(scratch))
     return o, lse
+
+
+def _expand_kv(x, H):
+    """[B, Hkv, N, d] -> [B, H, N, d]: query head h reads key/value head h // (H // Hkv)."""
+    x = _f64(x)
+    g = H // x.shape[1]
+    return np.repeat(x, g, axis=1)
+
+
+def fwd_gqa(q, k, v, bias=None, scale=None, causal=False):
+    """Grouped-query attention: every query head attends its group's key/value
+    head ("Understanding FlashAttention Pt 1", Part 4.1)."""
+    H = q.shape[1]
+    return fwd(q, _expand_kv(k, H), _expand_kv(v, H), bias=bias, scale=scale, causal=causal)
+
+
+def bwd_gqa(q, k, v, bias, dO, scale=None, causal=False):
+    """Backward of fwd_gqa: dK and dV of a shared head sum over its query heads."""
+    B, H = q.shape[0], q.shape[1]
+    Hkv = k.shape[1]
+    dq, dk, dv = bwd(q, _expand_kv(k, H), _expand_kv(v, H), bias, dO, scale=scale, causal=causal)
+    g = H // Hkv
+    dk = dk.reshape(B, Hkv, g, *dk.shape[2:]).sum(axis=2)
+    dv = dv.reshape(B, Hkv, g, *dv.shape[2:]).sum(axis=2)
+    return dq, dk, dv

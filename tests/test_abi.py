@@ -127,12 +127,23 @@ def test_splitkv_workspace_and_validation(lib):
     assert fa.fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, S) == r256(rows * d * 4) + r256(rows * 4)
     assert fa.fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, 0) == 0
     assert fa.fa_fwd_splitkv_default_splits(B, H, Nq, Nk, d) >= 1
-    a = dict(q=FAKE, k=FAKE, v=FAKE, key_bias=None, o=FAKE, lse=FAKE, B=B, H=H, Nq=Nq, Nk=Nk,
-             d=d, scale=0.1, causal=0, num_splits=S, workspace=FAKE, workspace_bytes=1 << 30,
-             stream=None)
+    a = dict(q=FAKE, k=FAKE, v=FAKE, key_bias=None, o=FAKE, lse=FAKE, B=B, H=H, H_kv=H, Nq=Nq,
+             Nk=Nk, d=d, scale=0.1, causal=0, num_splits=S, workspace=FAKE,
+             workspace_bytes=1 << 30, stream=None)
     for bad in (dict(num_splits=0), dict(workspace=None), dict(workspace_bytes=16),
-                dict(workspace=FAKE + 64), dict(lse=None), dict(d=80)):
+                dict(workspace=FAKE + 64), dict(lse=None), dict(d=80), dict(H_kv=2)):
         b = dict(a)
         b.update(bad)
         st = fa.fa_fwd_splitkv(**b)
         assert st in (fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED), bad
+
+
+@pytest.mark.parametrize("H,H_kv", [(8, 3), (8, 0), (4, 8), (4, -1)])
+def test_gqa_rejects_bad_head_counts(lib, H, H_kv):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, key_bias=None, o=FAKE, lse=FAKE, B=1, H=H, H_kv=H_kv, Nq=16,
+             Nk=16, d=64, scale=0.125, causal=0, dtype=fa.FA_DTYPE_BF16, stream=None)
+    assert fa.fa_fwd_gqa(**a) == fa.FA_ERR_INVALID_ARG
+    b = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dO=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             key_bias=None, B=1, H=H, H_kv=H_kv, Nq=16, Nk=16, d=64, scale=0.125, causal=1,
+             dtype=fa.FA_DTYPE_BF16, workspace=FAKE, workspace_bytes=1 << 20, stream=None)
+    assert fa.fa_bwd_gqa(**b) == fa.FA_ERR_INVALID_ARG

@@ -406,3 +406,45 @@ def test_row_sampled_backward_sums_to_full_backward():
     o, l = oracle.fwd_head_rows(q[0, 0], k[0, 0], v[0, 0], bias[0], [3, 12], 0.5, True)
     of, lf = oracle.fwd(q, k, v, bias=bias, scale=0.5, causal=True)
     np.testing.assert_allclose(o, of[0, 0, [3, 12]], atol=1e-15)
+
+
+# ------------------------------------------------------------- grouped heads
+
+def test_gqa_oracle_is_per_head_attention_on_the_shared_head():
+    B, H, Hkv, Nq, Nk, d = 2, 6, 2, 5, 9, 4
+    q, k, v = rand((B, H, Nq, d), 70), rand((B, Hkv, Nk, d), 71), rand((B, Hkv, Nk, d), 72)
+    o, lse = oracle.fwd_gqa(q, k, v, scale=0.5, causal=True)
+    for b in range(B):
+        for h in range(H):
+            kv = h // (H // Hkv)
+            oh, lh = oracle.fwd(q[b:b + 1, h:h + 1], k[b:b + 1, kv:kv + 1], v[b:b + 1, kv:kv + 1],
+                                scale=0.5, causal=True)
+            np.testing.assert_array_equal(o[b, h], oh[0, 0])
+            np.testing.assert_array_equal(lse[b, h], lh[0, 0])
+    o2, _ = oracle.fwd_gqa(q, np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1), scale=0.5,
+                           causal=True)
+    np.testing.assert_array_equal(o, o2)    # Hkv == H reduces to multi-head
+
+
+def test_gqa_backward_finite_differences_on_shared_heads():
+    B, H, Hkv, Nq, Nk, d = 1, 4, 2, 5, 6, 3
+    rng = np.random.default_rng(73)
+    q, k, v = (rng.standard_normal(s) for s in ((B, H, Nq, d), (B, Hkv, Nk, d), (B, Hkv, Nk, d)))
+    G = rng.standard_normal((B, H, Nq, d))
+
+    def loss(k_, v_):
+        o, _ = oracle.fwd_gqa(q, k_, v_, scale=0.6, causal=True)
+        return float((o * G).sum())
+
+    _, dk, dv = oracle.bwd_gqa(q, k, v, None, G, scale=0.6, causal=True)
+    h = 1e-6
+    for name, x, g in (("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            lp = loss(xp, v) if name == "k" else loss(k, xp)
+            lm = loss(xm, v) if name == "k" else loss(k, xm)
+            num[idx] = (lp - lm) / (2 * h)
+        assert np.abs(num - g).max() < 1e-6 * max(1.0, np.abs(g).max()), name

@@ -433,6 +433,67 @@ def run_ours(args):
         ms_g = b0.elapsed_time(b1) / n_e
         extras["gqa_b4h16kv4_n4096_d128_causal_fwdbwd_tflops"] = (f_fwd + f_bwd) / (ms_g * 1e-3) / 1e12
         del qg, dOg, kg, vg, og, lg, dqg, dkg, dvg
+        # packed variable-length batch vs the same batch padded to its longest sequence
+        lens = workloads.varlen_lengths(16, seed=2024)
+        Hv, dv_ = 16, 128
+        total, mx = sum(lens), max(lens)
+        cu = torch.tensor([0] + list(__import__("itertools").accumulate(lens)), dtype=torch.int32,
+                          device=dev)
+        qv, kv_, vv, dOv = (torch.randn((Hv, total, dv_), generator=g, device=dev,
+                                        dtype=torch.bfloat16) for _ in range(4))
+        ov = torch.empty_like(qv)
+        lv = torch.empty((Hv, total), dtype=torch.float32, device=dev)
+        dqv, dkv, dvv = torch.empty_like(qv), torch.empty_like(kv_), torch.empty_like(vv)
+        wsv = torch.empty(fa.fa_bwd_varlen_workspace_size(len(lens), Hv, total, mx, dv_),
+                          dtype=torch.uint8, device=dev)
+
+        def varlen_step():
+            fa.fwd_varlen(qv, kv_, vv, cu, cu, causal=True, out=ov, lse=lv, max_seqlen_q=mx,
+                          max_seqlen_k=mx)
+            fa.bwd_varlen(qv, kv_, vv, ov, lv, dOv, cu, cu, causal=True, workspace=wsv, dq=dqv,
+                          dk=dkv, dv=dvv, max_seqlen_q=mx, max_seqlen_k=mx)
+        for _ in range(3):
+            varlen_step()
+        b0.record(stream)
+        for _ in range(n_e):
+            varlen_step()
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        fa.check_device_error(dev)
+        ms_v = b0.elapsed_time(b1) / n_e
+        f_v = sum(3.5 * 4.0 * Hv * L * L * dv_ * 0.5 for L in lens)   # fwd + 2.5x bwd, causal
+        del qv, kv_, vv, dOv, ov, lv, dqv, dkv, dvv, wsv
+        # padded: B x max_len with the padding keys masked by the key bias
+        B_ = len(lens)
+        qp, kp, vp, dOp = (torch.randn((B_, Hv, mx, dv_), generator=g, device=dev,
+                                       dtype=torch.bfloat16) for _ in range(4))
+        bias_p = torch.zeros((B_, mx), dtype=torch.float32, device=dev)
+        for i, L in enumerate(lens):
+            bias_p[i, L:] = float("-inf")
+        op = torch.empty_like(qp)
+        lp = torch.empty(qp.shape[:3], dtype=torch.float32, device=dev)
+        dqp, dkp, dvp = torch.empty_like(qp), torch.empty_like(kp), torch.empty_like(vp)
+        wsp = torch.empty(fa.fa_bwd_workspace_size(B_, Hv, mx, mx, dv_), dtype=torch.uint8,
+                          device=dev)
+
+        def padded_step():
+            fa.fwd(qp, kp, vp, key_bias=bias_p, causal=True, out=op, lse=lp)
+            fa.bwd(qp, kp, vp, op, lp, dOp, key_bias=bias_p, causal=True, workspace=wsp, dq=dqp,
+                   dk=dkp, dv=dvp)
+        for _ in range(3):
+            padded_step()
+        b0.record(stream)
+        for _ in range(n_e):
+            padded_step()
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        fa.check_device_error(dev)
+        ms_p = b0.elapsed_time(b1) / n_e
+        extras["varlen_16seq_h16_d128_causal"] = {
+            "lengths": lens, "packed_ms": ms_v, "padded_ms": ms_p,
+            "packed_effective_tflops": f_v / (ms_v * 1e-3) / 1e12,
+            "padded_over_packed_time": ms_p / ms_v}
+        del qp, kp, vp, dOp, bias_p, op, lp, dqp, dkp, dvp, wsp
 
     if rank != 0:
         if world > 1:

@@ -52,6 +52,12 @@ def load(path=None):
     lib.fa_fwd_splitkv_default_splits.restype = cint
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint, cint, cf,
                                    cint, cint, vp, csz, vp]
+    lib.fa_fwd_varlen.argtypes = [vp] * 7 + [cint] * 8 + [cf, cint, vp]
+    lib.fa_fwd_varlen.restype = cint
+    lib.fa_bwd_varlen.argtypes = [vp] * 11 + [cint] * 8 + [cf, cint, vp, csz, vp]
+    lib.fa_bwd_varlen.restype = cint
+    lib.fa_bwd_varlen_workspace_size.argtypes = [cint] * 5
+    lib.fa_bwd_varlen_workspace_size.restype = csz
     lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint, cint, cf,
                                cint, cint, vp]
     lib.fa_fwd_gqa.restype = cint
@@ -85,6 +91,24 @@ def fa_fwd_splitkv(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, caus
                    workspace, workspace_bytes, stream):
     return load().fa_fwd_splitkv(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal,
                                  num_splits, workspace, workspace_bytes, stream)
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, H, H_kv, total_q, total_k,
+                  max_seqlen_q, max_seqlen_k, d, scale, causal, stream):
+    return load().fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, H, H_kv, total_q,
+                                total_k, max_seqlen_q, max_seqlen_k, d, scale, causal, stream)
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B, H, H_kv,
+                  total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale, causal, workspace,
+                  workspace_bytes, stream):
+    return load().fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B, H,
+                                H_kv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale,
+                                causal, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_q, d):
+    return load().fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_q, d)
 
 
 def fa_fwd_gqa(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal, dtype, stream):
@@ -244,6 +268,70 @@ def fwd_splitkv(q, k, v, key_bias=None, causal=False, scale=None, num_splits=Non
     if st != FA_OK:
         raise FaError(st, "fa_fwd_splitkv")
     return out, lse
+
+
+def _varlen_meta(cu_q, cu_k):
+    """B, total and max lengths of int32 offset tensors (read once on the host)."""
+    cq, ck = cu_q.detach().cpu().tolist(), cu_k.detach().cpu().tolist()
+    B = len(cq) - 1
+    return (B, cq[-1], ck[-1], max(cq[i + 1] - cq[i] for i in range(B)),
+            max(ck[i + 1] - ck[i] for i in range(B)))
+
+
+def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=None, out=None,
+               lse=None, max_seqlen_q=None, max_seqlen_k=None):
+    """Packed sequences: q [H, total_q, d], k/v [H_kv, total_k, d] bf16 CUDA tensors,
+    cu_seqlens int32 CUDA tensors [B+1]. Returns O [H, total_q, d], LSE [H, total_q]."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (cu_seqlens_q, "cu_seqlens_q"),
+                 (cu_seqlens_k, "cu_seqlens_k")):
+        _check(t, n)
+    H, total_q, d = q.shape
+    Hkv, total_k = k.shape[0], k.shape[1]
+    B, tq, tk, mq, mk = _varlen_meta(cu_seqlens_q, cu_seqlens_k)
+    max_seqlen_q = max(1, mq) if max_seqlen_q is None else max_seqlen_q
+    max_seqlen_k = max(1, mk) if max_seqlen_k is None else max_seqlen_k
+    if scale is None:
+        scale = d ** -0.5
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        st = fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                           _ptr(cu_seqlens_k), B, H, Hkv, total_q, total_k, max_seqlen_q,
+                           max_seqlen_k, d, float(scale), int(bool(causal)), _stream(q))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_varlen")
+    return out, lse
+
+
+def bwd_varlen(q, k, v, o, lse, dO, cu_seqlens_q, cu_seqlens_k, causal=False, scale=None,
+               workspace=None, dq=None, dk=None, dv=None, max_seqlen_q=None, max_seqlen_k=None):
+    """Backward of ``fwd_varlen`` (packed [H, total, d] tensors)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (dO, "dO")):
+        _check(t, n)
+    H, total_q, d = q.shape
+    Hkv, total_k = k.shape[0], k.shape[1]
+    B, tq, tk, mq, mk = _varlen_meta(cu_seqlens_q, cu_seqlens_k)
+    max_seqlen_q = max(1, mq) if max_seqlen_q is None else max_seqlen_q
+    max_seqlen_k = max(1, mk) if max_seqlen_k is None else max_seqlen_k
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_q, d),
+                                dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                           _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, H, Hkv,
+                           total_q, total_k, max_seqlen_q, max_seqlen_k, d, float(scale),
+                           int(bool(causal)), _ptr(workspace), workspace.numel(), _stream(q))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_varlen")
+    return dq, dk, dv
 
 
 def bwd(q, k, v, o, lse, dO, key_bias=None, causal=False, scale=None, workspace=None,

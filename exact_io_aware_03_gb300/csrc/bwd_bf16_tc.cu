@@ -52,25 +52,29 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
                                                       const float* __restrict__ lse,
                                                       float* __restrict__ Dv,
                                                       float* __restrict__ lse2,
-                                                      float* __restrict__ dq_acc, long BH,
-                                                      int Nq, int nq_pad) {
-  // Statistics are laid out per head with nq_pad (a multiple of 128) rows, so
-  // that every 128-row tile of them is one aligned 512-byte block; the padding
-  // rows get D = 0 and base-2 LSE = +inf (their recomputed P is exactly 0).
+                                                      float* __restrict__ dq_acc,
+                                                      const Problem p, int nq_pad,
+                                                      uint32_t* err) {
+  // Statistics are laid out per (sequence, head) with nq_pad (a multiple of
+  // 128) rows, so that every 128-row tile of them is one aligned 512-byte
+  // block; the padding rows get D = 0 and base-2 LSE = +inf (their recomputed
+  // P is exactly 0).
   constexpr int LPR = D / 8;          // lanes per row, 8 bf16 (16 B) per lane
   constexpr int RPW = 32 / LPR;       // rows per warp step
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, li = lane % LPR;
   const long warp_g = ((long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const long nwarps = ((long)gridDim.x * blockDim.x) / 32;
-  const long prows = BH * nq_pad;
+  const long prows = (long)p.B * p.H * nq_pad;
   for (long r0 = warp_g * RPW; r0 < prows; r0 += nwarps * RPW) {
-    const long pr = r0 + sub;            // padded row index
+    const long pr = r0 + sub;            // padded statistics row
     const bool in = pr < prows;
-    const long bh = pr / nq_pad;
-    const int i = (int)(pr - bh * nq_pad);
-    const bool valid = in && i < Nq;
-    const long row = bh * Nq + i;        // row of O, dO, LSE and the dQ accumulator
+    const int bh = (int)(min(pr, prows - 1) / nq_pad);
+    const int i = (int)(pr - (long)bh * nq_pad);
+    const SeqView sv = seq_view(p, bh / p.H, bh % p.H);
+    if (in && i == 0 && sv.bad) atomicOr(err, ERR_BAD_SEQLEN);
+    const bool valid = in && i < sv.len_q;
+    const long row = (long)sv.hq * sv.qrows + sv.q_off + i;   // row of O, dO, LSE, dQ accumulator
     float acc = 0.f;
     if (valid) {
       const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[li];
@@ -180,12 +184,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   const int jt = (int)(blockIdx.x % n_kt);
   const int b = bh_kv / p.Hkv;
   const int grp = p.H / p.Hkv;
-  const int bh_q0 = b * p.H + (bh_kv % p.Hkv) * grp;   // first query head of the group
+  const int h_q0 = (bh_kv % p.Hkv) * grp;   // first query head of the group
+  // rows and lengths of this sequence (keys and queries numbered from 0 in it)
+  const SeqView sv = seq_view(p, b, h_q0);
+  const int Nq = sv.len_q, Nk = sv.len_k;
   const int key0 = jt * kT;
-  const long off = (long)p.Nk - p.Nq;
+  const long off = (long)Nk - Nq;
 
   // ---- query tiles [i0, i1) that can see this key tile
-  const int n_qt = (p.Nq + kT - 1) / kT;
+  const int n_qt = (Nq + kT - 1) / kT;
   int i0 = 0;
   if (CAUSAL) {
     // smallest i with i*128 + 127 + off >= key0
@@ -195,7 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   const int i1 = n_qt;
   const int nqh = i1 - i0;   // query tiles per query head
   // query head and tile of step `it` of this CTA
-  auto q_head = [&](int it) { return bh_q0 + it / max(nqh, 1); };
+  // query head (within the batch) of step `it`, and its coordinate in q/dO/dq
+  auto q_head = [&](int it) { return h_q0 + it / max(nqh, 1); };
+  auto q_coord = [&](int h) { return p.cu_q ? h : b * p.H + h; };
   auto q_row0 = [&](int it) { return (i0 + it % max(nqh, 1)) * kT; };
 
   if (threadIdx.x == 0) {
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   float kb = -INFINITY;
   if (warp < 8) {
     const int key = key0 + (threadIdx.x & 127);
-    if (key < p.Nk) kb = BIAS ? a.bias[(size_t)b * p.Nk + key] * kLog2e : 0.f;
+    if (key < Nk) kb = BIAS ? a.bias[(size_t)b * Nk + key] * kLog2e : 0.f;
     if (kb != -INFINITY) *any_key = 1;
   }
   tc_fence_before();
@@ -241,20 +250,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     if (lane == 0 && n > 0) {
       mbar_arrive_expect_tx(bars.kv_full, 2 * C::TILE);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, key0, bh_kv, bars.kv_full);
-        tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, key0, bh_kv, bars.kv_full);
+        tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, sv.k_off + key0, sv.hk,
+                    bars.kv_full);
+        tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, sv.k_off + key0, sv.hk,
+                    bars.kv_full);
       }
       int nq = 0, nd = 0;   // Q / dO fills issued
       for (int it = 0; it < n; ++it) {
         const int s = it & 1, u = it >> 1;
-        const int q0 = q_row0(it), bh = q_head(it);
+        const int q0 = q_row0(it), hq = q_head(it);
         if (u > 0 && !wait1(&bars.q_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
         mbar_arrive_expect_tx(&bars.q_full[s], C::TILE + 2 * kT * 4);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * C::SUB, &a.tm_q, c * 64, q0, bh,
-                      &bars.q_full[s]);
+          tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * C::SUB, &a.tm_q, c * 64, sv.q_off + q0,
+                      q_coord(hq), &bars.q_full[s]);
         float* st = reinterpret_cast<float*>(smem + C::OFF_STAT) + s * 2 * kT;
-        const size_t srow = (size_t)bh * a.nq_pad + q0;
+        const size_t srow = ((size_t)b * p.H + hq) * a.nq_pad + q0;
         bulk_load_1d(st, a.lse2 + srow, kT * 4, &bars.q_full[s]);
         bulk_load_1d(st + kT, a.D + srow, kT * 4, &bars.q_full[s]);
         ++nq;
@@ -262,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         if (it > 0 && !wait1(bars.do_empty, (it - 1) & 1, wc, ERR_WAIT_LOAD)) break;
         mbar_arrive_expect_tx(bars.do_full, C::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_DO + c * C::SUB, &a.tm_do, c * 64, q0, bh, bars.do_full);
+          tma_load_3d(smem + C::OFF_DO + c * C::SUB, &a.tm_do, c * 64, sv.q_off + q0, q_coord(hq),
+                      bars.do_full);
         ++nd;
       }
       const WaitCtx wd{abort_flag, a.err, true};
@@ -379,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(bars.dq_empty);
-      const int row0 = q_row0(it) + (warp % 4) * 32;
-      const int bh = q_head(it);
+      const int row0 = sv.q_off + q_row0(it) + (warp % 4) * 32;
+      const int qc = q_coord(q_head(it));
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint8_t* stage = c == 0 ? stage0 : stage1;
@@ -399,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       if (lane == 0) {
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c)
-          tma_reduce_add_3d(&a.tm_dqacc, c == 0 ? stage0 : stage1, h * HD + c * 32, row0, bh);
+          tma_reduce_add_3d(&a.tm_dqacc, c == 0 ? stage0 : stage1, h * HD + c * 32, row0, qc);
       }
       if (lane == 0) bulk_commit_group();
       return true;
@@ -501,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // ---- dK, dV of this key tile (this warpgroup's half of the columns)
     if (ok && it == n) {
       const bool have = n > 0;
-      const size_t base = ((size_t)bh_kv * p.Nk + key) * D + h * HD;
+      const size_t base = ((size_t)sv.hk * sv.krows + sv.k_off + key) * D + h * HD;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {   // 0: dV, 1: dK
         uint16_t* dst = (which ? a.dk : a.dv) + base;
@@ -520,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
             pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]) * mul, __uint_as_float(x[e + 1]) * mul);
-          if (key < p.Nk) {
+          if (key < Nk) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
@@ -554,7 +566,8 @@ cudaError_t launch_main(const BwdBf16Args& a, cudaStream_t s) {
 
 template <int D>
 cudaError_t launch_d(const BwdBf16Args& a, cudaStream_t s, unsigned stages) {
-  const long rows = (long)a.p.B * a.p.H * a.p.Nq;
+  // rows of O, dO and the dQ accumulator
+  const long rows = a.p.cu_q ? (long)a.p.H * a.p.total_q : (long)a.p.B * a.p.H * a.p.Nq;
   cudaError_t e = cudaSuccess;
   if (stages & BWD_PRE) {
     constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
@@ -562,7 +575,7 @@ cudaError_t launch_d(const BwdBf16Args& a, cudaStream_t s, unsigned stages) {
     const long prows = BH * a.nq_pad;
     const long blocks = min((prows + kRowsPerBlock - 1) / kRowsPerBlock, (long)a.num_sms * 8);
     bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a.o, a.dO, a.lse, a.D, a.lse2, a.dq_acc,
-                                                      BH, a.p.Nq, a.nq_pad);
+                                                      a.p, a.nq_pad, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (stages & BWD_MAIN) {

@@ -109,6 +109,14 @@ fa_status make_map_f32_acc(CUtensorMap* m, const void* base, int BH, int N, int 
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace of the backward: padded statistics for B*H (sequence, head)
+// pairs of nq_max rows, then the fp32 dQ accumulator of `dq_rows` rows.
+size_t bwd_ws_bytes(int B, int H, int nq_max, size_t dq_rows, int d) {
+  const size_t prow = (size_t)B * H * (((size_t)nq_max + 127) / 128 * 128);
+  return 2 * round256(prow * 4) + round256(dq_rows * (size_t)d * 4);
+}
+
+
 // One thread waits (bounded) on an mbarrier that nothing ever arrives at, so
 // the wait runs out: it records FA_ERR_DEVICE's code in the error word and
 // returns, exactly as a stalled pipeline stage in the real kernels would.
@@ -121,6 +129,17 @@ __global__ void selftest_timeout_kernel(uint32_t* err) {
   fa::fence_mbar_init();
   const fa::WaitCtx w{&abort_flag, err};
   fa::wait1(&bar, 0, w, fa::ERR_WAIT_SOFTMAX);
+}
+
+// Shape checks of a packed variable-length batch (host side; the kernels
+// check every sequence's offsets and lengths against these bounds).
+fa_status check_varlen(int total_q, int total_k, int max_q, int max_k, int d, const int* cu_q,
+                       const int* cu_k) {
+  if (!cu_q || !cu_k || !aligned(cu_q, 4) || !aligned(cu_k, 4)) return FA_ERR_INVALID_ARG;
+  if (total_q < 1 || total_k < 1 || max_q > total_q || max_k > total_k) return FA_ERR_INVALID_ARG;
+  if ((long long)total_q * d >= (1LL << 31) || (long long)total_k * d >= (1LL << 31))
+    return FA_ERR_INVALID_ARG;
+  return FA_OK;
 }
 
 // Tensor maps and pointers of the bf16 forward (everything but the split).
@@ -185,6 +204,36 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, const float* k
   return fa::launch_fwd_bf16(a, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H, int H_kv,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                        float scale, int causal, void* stream) {
+  fa_status st = check_problem(B, H, max_seqlen_q, max_seqlen_k, d, scale, FA_DTYPE_BF16, H_kv);
+  if (st != FA_OK) return st;
+  st = check_varlen(total_q, total_k, max_seqlen_q, max_seqlen_k, d, cu_seqlens_q, cu_seqlens_k);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  fa::Problem p{B, H, max_seqlen_q, max_seqlen_k, d, scale, causal ? 1 : 0, H_kv};
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  fa::FwdBf16Args a;
+  std::memset(&a, 0, sizeof(a));
+  a.p = p;
+  if ((st = make_map(&a.tm_q, q, H, total_q, d)) != FA_OK) return st;
+  if ((st = make_map(&a.tm_k, k, H_kv, total_k, d)) != FA_OK) return st;
+  if ((st = make_map(&a.tm_v, v, H_kv, total_k, d)) != FA_OK) return st;
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
+  a.n_split = 1;
+  if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
+  return fa::launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                   : FA_ERR_CUDA;
+}
+
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || num_splits < 1) return 0;
   const size_t rows = (size_t)num_splits * B * H * Nq;
@@ -234,9 +283,12 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, const floa
 
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
-  const size_t rows = (size_t)B * H * Nq;
-  const size_t prow = (size_t)B * H * (((size_t)Nq + 127) / 128 * 128);   // 128-row padded
-  return 2 * round256(prow * 4) + round256(rows * (size_t)d * 4);
+  return bwd_ws_bytes(B, H, Nq, (size_t)B * H * Nq, d);
+}
+
+size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int max_seqlen_q, int d) {
+  if (B < 1 || H < 1 || total_q < 1 || max_seqlen_q < 1 || d < 1) return 0;
+  return bwd_ws_bytes(B, H, max_seqlen_q, (size_t)H * total_q, d);
 }
 
 }  // extern "C"
@@ -248,9 +300,14 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, void* dq, void* dk, void* dv,
                      const float* key_bias, int B, int H, int Hkv, int Nq, int Nk, int d,
                      float scale, int causal, fa_dtype dtype, void* workspace,
-                     size_t workspace_bytes, void* stream, unsigned stages) {
+                     size_t workspace_bytes, void* stream, unsigned stages,
+                     const int* cu_q = nullptr, const int* cu_k = nullptr, int total_q = 0,
+                     int total_k = 0) {
   fa_status st = check_problem(B, H, Nq, Nk, d, scale, dtype, Hkv);
   if (st != FA_OK) return st;
+  const bool varlen = cu_q != nullptr;
+  if (varlen && ((st = check_varlen(total_q, total_k, Nq, Nk, d, cu_q, cu_k)) != FA_OK)) return st;
+  if (varlen && key_bias) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
     return FA_ERR_INVALID_ARG;
@@ -259,29 +316,36 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
     if (!aligned(ptr, 16)) return FA_ERR_INVALID_ARG;
   if (!aligned(lse, 4) || (key_bias && !aligned(key_bias, 4)) || !aligned(workspace, 256))
     return FA_ERR_INVALID_ARG;
-  if (workspace_bytes < fa_bwd_workspace_size(B, H, Nq, Nk, d)) return FA_ERR_INVALID_ARG;
+  const size_t dq_rows = varlen ? (size_t)H * total_q : (size_t)B * H * Nq;
+  if (workspace_bytes < bwd_ws_bytes(B, H, Nq, dq_rows, d)) return FA_ERR_INVALID_ARG;
 
   fa::BwdBf16Args a;
   std::memset(&a, 0, sizeof(a));
   a.p = fa::Problem{B, H, Nq, Nk, d, scale, causal ? 1 : 0, Hkv};
-  const int BH = B * H;
+  a.p.cu_q = cu_q;
+  a.p.cu_k = cu_k;
+  a.p.total_q = total_q;
+  a.p.total_k = total_k;
+  // tensor-map views: (d, rows per head coordinate, head coordinates)
+  const int qh = varlen ? H : B * H, kh = varlen ? Hkv : B * Hkv;
+  const int qn = varlen ? total_q : Nq, kn = varlen ? total_k : Nk;
   if (stages & fa::BWD_MAIN) {
-    if ((st = make_map(&a.tm_q, q, BH, Nq, d)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_k, k, B * Hkv, Nk, d)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_v, v, B * Hkv, Nk, d)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_do, dO, BH, Nq, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_q, q, qh, qn, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_k, k, kh, kn, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_v, v, kh, kn, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_do, dO, qh, qn, d)) != FA_OK) return st;
   }
   a.o = static_cast<const uint16_t*>(o);
   a.dO = static_cast<const uint16_t*>(dO);
   a.lse = lse;
   a.bias = key_bias;
   a.nq_pad = (Nq + 127) / 128 * 128;
-  const size_t prow = (size_t)BH * a.nq_pad;
+  const size_t prow = (size_t)B * H * a.nq_pad;
   char* ws = static_cast<char*>(workspace);
   a.D = reinterpret_cast<float*>(ws);
   a.lse2 = reinterpret_cast<float*>(ws + round256(prow * 4));
   a.dq_acc = reinterpret_cast<float*>(ws + 2 * round256(prow * 4));
-  if ((stages & fa::BWD_MAIN) && (st = make_map_f32_acc(&a.tm_dqacc, a.dq_acc, BH, Nq, d)) != FA_OK)
+  if ((stages & fa::BWD_MAIN) && (st = make_map_f32_acc(&a.tm_dqacc, a.dq_acc, qh, qn, d)) != FA_OK)
     return st;
   a.dq = static_cast<uint16_t*>(dq);
   a.dk = static_cast<uint16_t*>(dk);
@@ -335,6 +399,19 @@ fa_status fa_bwd_postprocess(const void* q, const void* k, const void* v, const 
 }
 
 #undef FA_BWD_ARGS
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H, int H_kv,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                        float scale, int causal, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  if (!cu_seqlens_q) return FA_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, nullptr, B, H, H_kv, max_seqlen_q,
+                    max_seqlen_k, d, scale, causal, FA_DTYPE_BF16, workspace, workspace_bytes,
+                    stream, fa::BWD_PRE | fa::BWD_MAIN | fa::BWD_POST, cu_seqlens_q, cu_seqlens_k,
+                    total_q, total_k);
+}
 
 fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, void* dq, void* dk, void* dv,

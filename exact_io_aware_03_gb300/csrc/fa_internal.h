@@ -9,12 +9,51 @@ namespace fa {
 // Problem description shared by all kernels. q, o, dO, dq are [B][H][Nq][d];
 // k, v, dk, dv are [B][Hkv][Nk][d] with H a multiple of Hkv: query head h
 // attends key/value head h / (H / Hkv) (Hkv == H: plain multi-head).
+//
+// Packed variable-length batches (cu_q != nullptr): q, o, dO, dq are
+// [H][total_q][d], k, v, dk, dv are [Hkv][total_k][d], LSE is [H][total_q];
+// sequence b occupies rows [cu_q[b], cu_q[b+1]) of the queries and
+// [cu_k[b], cu_k[b+1]) of the keys, and Nq, Nk hold the largest lengths.
 struct Problem {
   int B, H, Nq, Nk, d;
   float scale;   // multiplies Q K^T
   int causal;    // bottom-right causal mask when non-zero
   int Hkv;       // key/value heads
+  const int* cu_q = nullptr;   // device int32 [B+1], or nullptr (dense)
+  const int* cu_k = nullptr;
+  int total_q = 0, total_k = 0;
 };
+
+// Where the rows of sequence b, query head h live (see Problem).
+struct SeqView {
+  int q_off, len_q, k_off, len_k;   // row offsets inside the head's rows, lengths
+  int hq, hk;                       // head coordinate of q/o/lse and of k/v rows
+  long qrows, krows;                // rows per head coordinate
+  bool bad;                         // a length outside [0, Nq] x [0, Nk]
+};
+
+__device__ __forceinline__ SeqView seq_view(const Problem& p, int b, int h) {
+  SeqView v;
+  const int hkv = h / (p.H / p.Hkv);
+  if (p.cu_q == nullptr) {
+    v.q_off = 0; v.len_q = p.Nq; v.k_off = 0; v.len_k = p.Nk;
+    v.hq = b * p.H + h; v.hk = b * p.Hkv + hkv;
+    v.qrows = p.Nq; v.krows = p.Nk;
+    v.bad = false;
+    return v;
+  }
+  v.q_off = p.cu_q[b];
+  v.len_q = p.cu_q[b + 1] - v.q_off;
+  v.k_off = p.cu_k[b];
+  v.len_k = p.cu_k[b + 1] - v.k_off;
+  v.hq = h; v.hk = hkv;
+  v.qrows = p.total_q; v.krows = p.total_k;
+  v.bad = v.len_q < 0 || v.len_q > p.Nq || v.len_k < 0 || v.len_k > p.Nk || v.q_off < 0 ||
+          v.k_off < 0 || (long)v.q_off + v.len_q > p.total_q ||
+          (long)v.k_off + v.len_k > p.total_k;
+  if (v.bad) { v.len_q = 0; v.len_k = 0; v.q_off = 0; v.k_off = 0; }
+  return v;
+}
 
 struct FwdF32Args {
   Problem p;

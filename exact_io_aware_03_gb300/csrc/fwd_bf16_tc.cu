@@ -140,9 +140,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   const int bh = g0 + rr % gsz;
   const int pair = n_pairs - 1 - rr / gsz;
   const int b = bh / p.H;
-  const int bh_kv = b * p.Hkv + (bh % p.H) / (p.H / p.Hkv);   // key/value head of this query head
+  // rows, lengths and head coordinates of this (sequence, head); query rows
+  // and keys are numbered from 0 inside the sequence below
+  const SeqView sv = seq_view(p, b, bh % p.H);
+  const int Nq = sv.len_q, Nk = sv.len_k;
   const int q_base = pair * 2 * kBM;
-  const float* bias_row = BIAS ? a.bias + (size_t)b * p.Nk : nullptr;
+  const float* bias_row = BIAS ? a.bias + (size_t)b * Nk : nullptr;
 
   // ---- set-up: barriers, TMEM, optional scan of the bias row
   if (threadIdx.x == 0) {
@@ -163,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     }
     mbar_init(bars.drain, 1);
     *abort_flag = 0;
-    *key_lo_s = p.Nk;
+    *key_lo_s = Nk;
+    if (sv.bad && pair == n_pairs - 1) atomicOr(a.err, ERR_BAD_SEQLEN);
     *key_hi_s = -1;
     fence_mbar_init();
   }
@@ -179,14 +183,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   __syncthreads();
   if (BIAS) {
     // first and last key with a finite bias; tiles outside are skipped
-    int lo = p.Nk, hi = -1;
-    for (int j = threadIdx.x; j < p.Nk; j += kThreads) {
+    int lo = Nk, hi = -1;
+    for (int j = threadIdx.x; j < Nk; j += kThreads) {
       if (bias_row[j] != -INFINITY) {
         lo = min(lo, j);
         hi = max(hi, j);
       }
     }
-    if (lo < p.Nk) atomicMin(key_lo_s, lo);
+    if (lo < Nk) atomicMin(key_lo_s, lo);
     if (hi >= 0) atomicMax(key_hi_s, hi);
   }
   tc_fence_before();
@@ -195,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
 
   // ---- key-tile ranges [lo, hi_t) of the two query tiles
-  const int n_kv = (p.Nk + kBN - 1) / kBN;
+  const int n_kv = (Nk + kBN - 1) / kBN;
   int lo = 0, hi_all = n_kv;
   if (BIAS) {
     const int klo = *key_lo_s, khi = *key_hi_s;
@@ -211,11 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   for (int t = 0; t < 2; ++t) {
     const int r0 = q_base + t * kBM;
     int h = hi_all;
-    if (r0 >= p.Nq) {
+    if (r0 >= Nq) {
       h = lo;   // tile past the last query row: inactive
     } else if (CAUSAL) {
-      const long last_row = min(r0 + kBM - 1, p.Nq - 1);
-      const long lim = last_row + (long)p.Nk - p.Nq;
+      const long last_row = min(r0 + kBM - 1, Nq - 1);
+      const long lim = last_row + (long)Nk - Nq;
       h = lim < 0 ? 0 : (int)min((long)hi_all, lim / kBN + 1);
     }
     hi_t[t] = max(h, lo);
@@ -239,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         if (hi_t[t] <= lo) continue;
         mbar_arrive_expect_tx(&bars.q_full[t], C::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(q_s + t * C::TILE + c * C::SUB, &a.tm_q, c * 64, q_base + t * kBM, bh,
+          tma_load_3d(q_s + t * C::TILE + c * C::SUB, &a.tm_q, c * 64, sv.q_off + q_base + t * kBM,
+                      sv.hq,
                       &bars.q_full[t]);
       }
       int nk = 0, nv = 0;   // K / V fills issued
@@ -248,13 +253,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         if (u > 0 && !wait1(&bars.k_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
         mbar_arrive_expect_tx(&bars.k_full[s], C::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::SUB, &a.tm_k, c * 64, j * kBN, bh_kv,
+          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::SUB, &a.tm_k, c * 64,
+                      sv.k_off + j * kBN, sv.hk,
                       &bars.k_full[s]);
         ++nk;
         if (u > 0 && !wait1(&bars.v_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
         mbar_arrive_expect_tx(&bars.v_full[s], C::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::SUB, &a.tm_v, c * 64, j * kBN, bh_kv,
+          tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::SUB, &a.tm_v, c * 64,
+                      sv.k_off + j * kBN, sv.hk,
                       &bars.v_full[s]);
         ++nv;
       }
@@ -347,11 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const uint32_t s_col = t * 128, o_col = 256 + t * D;
     const float sl2 = p.scale * kLog2e;
-    const long off = (long)p.Nk - p.Nq;
+    const long off = (long)Nk - Nq;
     // last visible key of this row / of the tile's first row (tile-uniform)
-    const long lim_row = CAUSAL ? min((long)row_g + off, (long)p.Nk - 1) : (long)p.Nk - 1;
+    const long lim_row = CAUSAL ? min((long)row_g + off, (long)Nk - 1) : (long)Nk - 1;
     const long lim_tile =
-        CAUSAL ? min((long)(q_base + t * kBM) + off, (long)p.Nk - 1) : (long)p.Nk - 1;
+        CAUSAL ? min((long)(q_base + t * kBM) + off, (long)Nk - 1) : (long)Nk - 1;
     float m = -INFINITY, l = 0.f;
     const int n_t = hi_t[t] - lo;
     int i = 0;
@@ -361,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       if (BIAS) {
         float* bb = bias_buf + (t * 2 + (i & 1)) * kBN;
         const int kj = key0 + r;
-        bb[r] = kj < p.Nk ? bias_row[kj] * kLog2e : -INFINITY;
+        bb[r] = kj < Nk ? bias_row[kj] * kLog2e : -INFINITY;
         mbar_arrive(&bars.bias_rdy[t * 2 + (i & 1)]);
         if (!wait_warp(&bars.bias_rdy[t * 2 + (i & 1)], (i >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) break;
       }
@@ -473,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
 #pragma unroll
           for (int c = 0; c < 32; ++c) ov[c] = 0u;
         }
-        if (row_g < p.Nq) {
+        if (row_g < Nq) {
           float4* dst = reinterpret_cast<float4*>(orow + c0);
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4)
@@ -482,10 +489,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                                   __uint_as_float(ov[4 * v4 + 3]) * inv);
         }
       }
-      if (row_g < p.Nq) a.part_lse[prow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (row_g < Nq) a.part_lse[prow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     } else if (completed) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* orow = a.o + ((size_t)bh * p.Nq + row_g) * D;
+      const size_t orow_idx = (size_t)sv.hq * sv.qrows + sv.q_off + row_g;
+      uint16_t* orow = a.o + orow_idx * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t ov[32];
@@ -500,15 +508,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
 #pragma unroll
         for (int c = 0; c < 32; c += 2)
           pk[c / 2] = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
-        if (row_g < p.Nq) {
+        if (row_g < Nq) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
             dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
         }
       }
-      if (row_g < p.Nq)
-        a.lse[(size_t)bh * p.Nq + row_g] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (row_g < Nq) a.lse[orow_idx] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 

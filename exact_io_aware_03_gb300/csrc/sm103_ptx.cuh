@@ -23,6 +23,7 @@ enum : uint32_t {
   ERR_WAIT_SOFTMAX = 1u << 2,  // softmax warps timed out waiting for S / O
   ERR_WAIT_EPILOGUE = 1u << 3, // epilogue warps timed out
   ERR_WAIT_DRAIN = 1u << 4,    // final drain of in-flight copies/MMAs timed out
+  ERR_BAD_SEQLEN = 1u << 5,    // a packed sequence's offsets/lengths are out of range
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -102,6 +102,40 @@ fa_status fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
                      fa_dtype dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Packed variable-length batches ("flash-attention", the varlen entry points
+ * with cu_seqlens; padding replaced by packing): B sequences of different
+ * lengths are stored back to back, per head:
+ *   q, o: [H][total_q][d] bf16   k, v: [H_kv][total_k][d] bf16   lse: [H][total_q]
+ * Sequence b occupies query rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key
+ * rows [cu_seqlens_k[b], cu_seqlens_k[b+1]) (device int32 arrays of B+1
+ * non-decreasing offsets, cu[0] = 0, cu[B] = total). Each sequence is an
+ * independent problem: causal is bottom-right within the sequence, and no
+ * query attends keys of another sequence. max_seqlen_q/k must be at least
+ * the largest sequence length (they size the grid). A sequence whose offsets
+ * or length break these rules is detected on the device and reported by
+ * fa_get_last_device_error (its rows are then not written). No key bias.
+ */
+fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                        const int *cu_seqlens_q, const int *cu_seqlens_k,
+                        int B, int H, int H_kv, int total_q, int total_k,
+                        int max_seqlen_q, int max_seqlen_k, int d, float scale, int causal,
+                        void *stream);
+
+/*
+ * Backward of fa_fwd_varlen (same packed layout; o and lse from that call;
+ * dq [H][total_q][d], dk, dv [H_kv][total_k][d]). Workspace:
+ * fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_q, d) bytes,
+ * 256-byte aligned.
+ */
+size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int max_seqlen_q, int d);
+fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                        const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                        const int *cu_seqlens_q, const int *cu_seqlens_k,
+                        int B, int H, int H_kv, int total_q, int total_k,
+                        int max_seqlen_q, int max_seqlen_k, int d, float scale, int causal,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Split-KV forward (Flash-Decoding) for problems with few query rows and many
  * keys, e.g. decoding: the keys of every (b, h) are cut into num_splits
  * contiguous ranges processed by separate CTAs, each producing a partial

@@ -272,3 +272,43 @@ def bwd_gqa(q, k, v, bias, dO, scale=None, causal=False):
     dk = dk.reshape(B, Hkv, g, *dk.shape[2:]).sum(axis=2)
     dv = dv.reshape(B, Hkv, g, *dv.shape[2:]).sum(axis=2)
     return dq, dk, dv
+
+
+def fwd_varlen(q, k, v, cu_q, cu_k, scale=None, causal=False):
+    """Packed sequences (q [H, total_q, d], k/v [H_kv, total_k, d], offsets [B+1]):
+    each sequence is its own problem; returns O [H, total_q, d], LSE [H, total_q]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cu_q = [int(x) for x in np.asarray(cu_q).reshape(-1)]
+    cu_k = [int(x) for x in np.asarray(cu_k).reshape(-1)]
+    H, total_q, d = q.shape
+    o = np.zeros((H, total_q, d))
+    lse = np.full((H, total_q), -np.inf)
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if q1 == q0:
+            continue
+        if k1 == k0:
+            continue    # no key at all: O = 0, LSE = -inf
+        ob, lb = fwd_gqa(q[None, :, q0:q1], k[None, :, k0:k1], v[None, :, k0:k1], scale=scale,
+                         causal=causal)
+        o[:, q0:q1] = ob[0]
+        lse[:, q0:q1] = lb[0]
+    return o, lse
+
+
+def bwd_varlen(q, k, v, dO, cu_q, cu_k, scale=None, causal=False):
+    """Backward of fwd_varlen: dQ [H, total_q, d], dK, dV [H_kv, total_k, d]."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    cu_q = [int(x) for x in np.asarray(cu_q).reshape(-1)]
+    cu_k = [int(x) for x in np.asarray(cu_k).reshape(-1)]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if q1 == q0 or k1 == k0:
+            continue
+        gq, gk, gv = bwd_gqa(q[None, :, q0:q1], k[None, :, k0:k1], v[None, :, k0:k1], None,
+                             dO[None, :, q0:q1], scale=scale, causal=causal)
+        dq[:, q0:q1] = gq[0]
+        dk[:, k0:k1] = gk[0]
+        dv[:, k0:k1] = gv[0]
+    return dq, dk, dv

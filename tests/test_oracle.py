@@ -448,3 +448,35 @@ def test_gqa_backward_finite_differences_on_shared_heads():
             lm = loss(xm, v) if name == "k" else loss(k, xm)
             num[idx] = (lp - lm) / (2 * h)
         assert np.abs(num - g).max() < 1e-6 * max(1.0, np.abs(g).max()), name
+
+
+# ------------------------------------------------------------- packed sequences
+
+def test_varlen_oracle_equal_lengths_is_the_dense_batch():
+    B, H, N, d = 3, 2, 7, 4
+    q, k, v = rand((B, H, N, d), 80), rand((B, H, N, d), 81), rand((B, H, N, d), 82)
+    pack = lambda x: np.concatenate([x[b] for b in range(B)], axis=1)   # [H, B*N, d]
+    cu = np.arange(0, (B + 1) * N, N)
+    o, lse = oracle.fwd_varlen(pack(q), pack(k), pack(v), cu, cu, scale=0.4, causal=True)
+    od, ld = oracle.fwd(q, k, v, scale=0.4, causal=True)
+    np.testing.assert_array_equal(o, pack(od))
+    np.testing.assert_array_equal(lse, np.concatenate([ld[b] for b in range(B)], axis=1))
+    G = rand((B, H, N, d), 83)
+    dq, dk, dv = oracle.bwd_varlen(pack(q), pack(k), pack(v), pack(G), cu, cu, scale=0.4,
+                                   causal=True)
+    dqd, dkd, dvd = oracle.bwd(q, k, v, None, G, scale=0.4, causal=True)
+    np.testing.assert_allclose(dq, pack(dqd), atol=1e-15)
+    np.testing.assert_allclose(dk, pack(dkd), atol=1e-15)
+
+
+def test_varlen_oracle_sequences_do_not_interact():
+    H, d = 2, 4
+    lens = [3, 0, 5]
+    total = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q, k, v = rand((H, total, d), 84), rand((H, total, d), 85), rand((H, total, d), 86)
+    o, _ = oracle.fwd_varlen(q, k, v, cu, cu, scale=1.0)
+    v2 = v.copy()
+    v2[:, 3:] += 100.0            # change only the last sequence's values
+    o2, _ = oracle.fwd_varlen(q, k, v2, cu, cu, scale=1.0)
+    np.testing.assert_array_equal(o[:, :3], o2[:, :3])

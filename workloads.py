@@ -112,3 +112,12 @@ def sample_rows(w: Workload, n: int, seed: int = 7):
     heads = torch.cat([heads, torch.tensor([0, w.B * w.H - 1])])
     rows = torch.cat([rows, torch.tensor([w.Nq - 1, w.Nq - 1])])
     return heads.numpy(), rows.numpy()
+
+
+def varlen_lengths(n: int, seed: int, cap: int = 4096, lo: int = 64):
+    """n sequence lengths drawn from a log-normal (median ~1000) clipped to
+    [lo, cap] -- the ragged-batch shape used to compare packed and padded
+    batches. Returns a list of ints."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.exp(torch.randn(n, generator=g, dtype=torch.float64) * 0.8 + math.log(1000.0))
+    return [int(v) for v in x.clamp(lo, cap).round().tolist()]

@@ -433,6 +433,36 @@ def run_ours(args):
         ms_g = b0.elapsed_time(b1) / n_e
         extras["gqa_b4h16kv4_n4096_d128_causal_fwdbwd_tflops"] = (f_fwd + f_bwd) / (ms_g * 1e-3) / 1e12
         del qg, dOg, kg, vg, og, lg, dqg, dkg, dvg
+        # deterministic backward (query-outer dQ kernel, no reductions) on the
+        # benchmark workload, timed per launch
+        wsd = torch.empty(fa.fa_bwd_deterministic_workspace_size(w.B, w.H, w.Nq, w.d),
+                          dtype=torch.uint8, device=dev)
+        det_stages = ("preprocess", "dkdv", "dq")
+
+        def det_bwd(ev=None):
+            for i, st in enumerate(det_stages):
+                if ev is not None:
+                    ev[i].record(stream)
+                fa.bwd(q, k, v, o, lse, dO, workspace=wsd, dq=dq, dk=dk, dv=dv,
+                       deterministic=True, stage=st, **kw)
+            if ev is not None:
+                ev[3].record(stream)
+        fa.fwd(q, k, v, out=o, lse=lse, **kw)
+        for _ in range(3):
+            det_bwd()
+        evd = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_e)]
+        for i in range(n_e):
+            det_bwd(evd[i])
+        torch.cuda.synchronize(dev)
+        fa.check_device_error(dev)
+        det_ms = {st: statistics.median(e[i].elapsed_time(e[i + 1]) for e in evd)
+                  for i, st in enumerate(det_stages)}
+        det_total = statistics.median(e[0].elapsed_time(e[3]) for e in evd)
+        extras["deterministic_bwd_" + w.name] = {
+            "ms": det_total, "stages_ms": det_ms,
+            "tflops": f_bwd / (det_total * 1e-3) / 1e12,
+            "flop_convention": "same 2.5x-forward count as fa_bwd (the kernels do 7/5 of it)"}
+        del wsd
         # packed variable-length batch vs the same batch padded to its longest sequence
         lens = workloads.varlen_lengths(16, seed=2024)
         Hv, dv_ = 16, 128
@@ -559,7 +589,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the forward-only long-context measurement")
+                    help="skip the extra measurements (long-context forward, decode, GQA, ragged batch)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

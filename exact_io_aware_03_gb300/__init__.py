@@ -65,6 +65,14 @@ def load(path=None):
                                cint, cint, cf, cint, cint, vp, csz, vp]
     lib.fa_bwd_gqa.restype = cint
     lib.fa_fwd_splitkv.restype = cint
+    lib.fa_bwd_deterministic_workspace_size.argtypes = [cint] * 4
+    lib.fa_bwd_deterministic_workspace_size.restype = csz
+    lib.fa_bwd_deterministic.argtypes = list(lib.fa_bwd_gqa.argtypes)
+    lib.fa_bwd_deterministic.restype = cint
+    lib.fa_bwd_deterministic_stage.argtypes = list(lib.fa_bwd_gqa.argtypes) + [cint]
+    lib.fa_bwd_deterministic_stage.restype = cint
+    lib.fa_bwd_varlen_deterministic.argtypes = list(lib.fa_bwd_varlen.argtypes)
+    lib.fa_bwd_varlen_deterministic.restype = cint
     for name in ("fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess"):
         f = getattr(lib, name)
         f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint,
@@ -120,6 +128,33 @@ def fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d,
                dtype, workspace, workspace_bytes, stream):
     return load().fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d,
                              scale, causal, dtype, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_deterministic_workspace_size(B, H, Nq, d):
+    return load().fa_bwd_deterministic_workspace_size(B, H, Nq, d)
+
+
+def fa_bwd_deterministic(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d, scale,
+                         causal, dtype, workspace, workspace_bytes, stream):
+    return load().fa_bwd_deterministic(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq,
+                                       Nk, d, scale, causal, dtype, workspace, workspace_bytes,
+                                       stream)
+
+
+def fa_bwd_deterministic_stage(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d,
+                               scale, causal, dtype, workspace, workspace_bytes, stream, stage):
+    return load().fa_bwd_deterministic_stage(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H,
+                                             H_kv, Nq, Nk, d, scale, causal, dtype, workspace,
+                                             workspace_bytes, stream, stage)
+
+
+def fa_bwd_varlen_deterministic(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B, H,
+                                H_kv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale,
+                                causal, workspace, workspace_bytes, stream):
+    return load().fa_bwd_varlen_deterministic(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q,
+                                              cu_seqlens_k, B, H, H_kv, total_q, total_k,
+                                              max_seqlen_q, max_seqlen_k, d, scale, causal,
+                                              workspace, workspace_bytes, stream)
 
 
 def fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits):
@@ -306,8 +341,12 @@ def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=None, ou
 
 
 def bwd_varlen(q, k, v, o, lse, dO, cu_seqlens_q, cu_seqlens_k, causal=False, scale=None,
-               workspace=None, dq=None, dk=None, dv=None, max_seqlen_q=None, max_seqlen_k=None):
-    """Backward of ``fwd_varlen`` (packed [H, total, d] tensors)."""
+               workspace=None, dq=None, dk=None, dv=None, max_seqlen_q=None, max_seqlen_k=None,
+               deterministic=False):
+    """Backward of ``fwd_varlen`` (packed [H, total, d] tensors).
+
+    deterministic: use fa_bwd_varlen_deterministic (bitwise reproducible dq).
+    """
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (dO, "dO")):
         _check(t, n)
@@ -322,24 +361,28 @@ def bwd_varlen(q, k, v, o, lse, dO, cu_seqlens_q, cu_seqlens_k, causal=False, sc
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     if workspace is None:
-        workspace = torch.empty(fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_q, d),
-                                dtype=torch.uint8, device=q.device)
+        nbytes = (fa_bwd_deterministic_workspace_size(B, H, max_seqlen_q, d) if deterministic
+                  else fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_q, d))
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    fn = fa_bwd_varlen_deterministic if deterministic else fa_bwd_varlen
     with torch.cuda.device(q.device):
-        st = fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+        st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
                            _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, H, Hkv,
                            total_q, total_k, max_seqlen_q, max_seqlen_k, d, float(scale),
                            int(bool(causal)), _ptr(workspace), workspace.numel(), _stream(q))
     if st != FA_OK:
-        raise FaError(st, "fa_bwd_varlen")
+        raise FaError(st, fn.__name__)
     return dq, dk, dv
 
 
 def bwd(q, k, v, o, lse, dO, key_bias=None, causal=False, scale=None, workspace=None,
-        dq=None, dk=None, dv=None, stage=None):
+        dq=None, dk=None, dv=None, stage=None, deterministic=False):
     """dQ, dK, dV (q's dtype) for CUDA tensors; o and lse from ``fwd`` on the same inputs.
 
     stage: None runs the whole backward (fa_bwd); "preprocess", "main" or
     "postprocess" runs only that launch (the three in order equal fa_bwd).
+    deterministic: use fa_bwd_deterministic (bitwise reproducible dq); its
+    stages are "preprocess", "dkdv" and "dq".
     """
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (dO, "dO")):
@@ -351,9 +394,25 @@ def bwd(q, k, v, o, lse, dO, key_bias=None, causal=False, scale=None, workspace=
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws_bytes = fa_bwd_workspace_size(B, H, Nq, Nk, d)
+    ws_bytes = (fa_bwd_deterministic_workspace_size(B, H, Nq, d) if deterministic
+                else fa_bwd_workspace_size(B, H, Nq, Nk, d))
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    if deterministic:
+        extra = ()
+        if stage is None:
+            fn = fa_bwd_deterministic
+        else:
+            fn = fa_bwd_deterministic_stage
+            extra = ({"preprocess": 1, "dkdv": 2, "dq": 3}[stage],)
+        with torch.cuda.device(q.device):
+            st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                    _ptr(dk), _ptr(dv), _ptr(key_bias), B, H, Hkv, Nq, Nk, d, float(scale),
+                    int(bool(causal)), _dtype_code(q), _ptr(workspace), workspace.numel(),
+                    _stream(q), *extra)
+        if st != FA_OK:
+            raise FaError(st, fn.__name__)
+        return dq, dk, dv
     if stage is None:
         fn = fa_bwd_gqa
         heads = (B, H, Hkv)

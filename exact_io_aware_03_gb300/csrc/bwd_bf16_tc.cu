@@ -21,6 +21,13 @@
 //     in TMEM until the last query tile and are written once, scaled.
 //  3. bwd_post: dQ = bf16(accumulator).
 //
+// Deterministic variant (DET): bwd_main runs without the dQ product; dS^T
+// goes to TMEM as packed bf16 (next to P^T's place, in the dP^T columns) and
+// dK += dS^T Q reads it from there like dV reads P^T. dQ is then formed by
+// the query-outer kernel of bwd_dq_tc.cu, which sums the key tiles in a fixed
+// order; there is no accumulator to zero and no bwd_post. dO is double-buffered
+// in the shared memory the dS and staging buffers used.
+//
 // Warp roles of bwd_main (320 threads): warps 0-7 are two warpgroups that
 // split the query columns of every tile; they compute P^T (kept in fp32
 // registers) and dS^T (thread = key = TMEM lane), read dQ_i out of TMEM
@@ -86,9 +93,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
         acc = fmaf(__uint_as_float(av[e] & 0xffff0000u), __uint_as_float(gv[e] & 0xffff0000u),
                    acc);
       }
-      float4* z = reinterpret_cast<float4*>(dq_acc + row * D);
-      z[2 * li] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[2 * li + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (dq_acc) {
+        float4* z = reinterpret_cast<float4*>(dq_acc + row * D);
+        z[2 * li] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[2 * li + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
     for (int w = LPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
@@ -111,21 +120,21 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
 }
 
 // ------------------------------------------------------------------ main
-template <int D>
+template <int D, bool DET>
 struct BwdCfg {
   static constexpr int TILE = kT * D * 2;     // bf16 [128][D]
   static constexpr int SUB = kT * 128;        // one 64-column box
-  static constexpr int DS_BYTES = kT * kT * 2;
+  static constexpr int ND = DET ? 2 : 1;      // dO stages
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
   static constexpr int OFF_Q = OFF_V + TILE;         // [2 stages]
-  static constexpr int OFF_DO = OFF_Q + 2 * TILE;    // [1 stage]
-  static constexpr int OFF_DQST = OFF_DO + TILE;     // 32 KiB: second dQ staging slice
-  static constexpr int OFF_DS = OFF_DQST + 32768;
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;    // [ND stages]
+  static constexpr int OFF_DQST = OFF_DO + ND * TILE;               // 32 KiB: second dQ staging slice
+  static constexpr int OFF_DS = OFF_DQST + (DET ? 0 : 32768);       // dS^T boxes
   // per Q stage: base-2 LSE [128] then D [128] of the tile's rows (TMA)
-  static constexpr int OFF_STAT = OFF_DS + DS_BYTES;
+  static constexpr int OFF_STAT = OFF_DS + (DET ? 0 : kT * kT * 2);
   static constexpr int OFF_BAR = OFF_STAT + 2 * 2 * kT * 4;
-  static constexpr int NBAR = 1 + 2 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 1;
+  static constexpr int NBAR = 1 + 2 + 2 + 2 * ND + 1 + 1 + 1 + 1 + 1 + 1 + 1;
   static constexpr int OFF_SCALARS = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_SCALARS + 32;
 };
@@ -134,21 +143,21 @@ struct BwdBars {
   uint64_t* kv_full;   // [1]
   uint64_t* q_full;    // [2]  Q_i and its base-2 LSE and D of a stage
   uint64_t* q_empty;   // [2]
-  uint64_t* do_full;   // dO_i (single buffer)
-  uint64_t* do_empty;
+  uint64_t* do_full;   // [ND] dO_i
+  uint64_t* do_empty;  // [ND]
   uint64_t* s_full;    // S^T done
   uint64_t* dp_full;   // dP^T done
   uint64_t* p_full;    // P^T in TMEM (128 arrivals)
   uint64_t* ds_full;   // dS^T in TMEM + smem (128 arrivals)
-  uint64_t* dq_full;   // dQ_i done (and everything before it)
+  uint64_t* dq_full;   // dQ_i done (and everything before it); DET: the last dK done
   uint64_t* dq_empty;  // dQ_i read out of TMEM (128 arrivals)
   uint64_t* drain;
 };
 
 
-template <int D, bool CAUSAL, bool BIAS>
+template <int D, bool CAUSAL, bool BIAS, bool DET>
 __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdBf16Args a) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, DET>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const Problem& p = a.p;
   const int warp = threadIdx.x / 32;
@@ -159,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   bars.kv_full = bb; bb += 1;
   bars.q_full = bb; bb += 2;
   bars.q_empty = bb; bb += 2;
-  bars.do_full = bb; bb += 1;
-  bars.do_empty = bb; bb += 1;
+  bars.do_full = bb; bb += C::ND;
+  bars.do_empty = bb; bb += C::ND;
   bars.s_full = bb; bb += 1;
   bars.dp_full = bb; bb += 1;
   bars.p_full = bb; bb += 1;
@@ -214,8 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
     }
-    mbar_init(bars.do_full, 1);
-    mbar_init(bars.do_empty, 1);
+    for (int s = 0; s < C::ND; ++s) {
+      mbar_init(&bars.do_full[s], 1);
+      mbar_init(&bars.do_empty[s], 1);
+    }
     mbar_init(bars.s_full, 1);
     mbar_init(bars.dp_full, 1);
     mbar_init(bars.p_full, 2 * kT);
@@ -269,19 +280,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         bulk_load_1d(st, a.lse2 + srow, kT * 4, &bars.q_full[s]);
         bulk_load_1d(st + kT, a.D + srow, kT * 4, &bars.q_full[s]);
         ++nq;
-        // dO has one buffer: its next tile may land once dV of this one is done
-        if (it > 0 && !wait1(bars.do_empty, (it - 1) & 1, wc, ERR_WAIT_LOAD)) break;
-        mbar_arrive_expect_tx(bars.do_full, C::TILE);
+        // dO stage sd may be refilled once dV of its previous tile is done
+        const int sd = it % C::ND, ud = it / C::ND;
+        if (ud > 0 && !wait1(&bars.do_empty[sd], (ud - 1) & 1, wc, ERR_WAIT_LOAD)) break;
+        mbar_arrive_expect_tx(&bars.do_full[sd], C::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_DO + c * C::SUB, &a.tm_do, c * 64, sv.q_off + q0, q_coord(hq),
-                      bars.do_full);
+          tma_load_3d(smem + C::OFF_DO + sd * C::TILE + c * C::SUB, &a.tm_do, c * 64,
+                      sv.q_off + q0, q_coord(hq), &bars.do_full[sd]);
         ++nd;
       }
       const WaitCtx wd{abort_flag, a.err, true};
       wait1(bars.kv_full, 0, wd, ERR_WAIT_DRAIN);
       for (int it = max(0, nq - 2); it < nq; ++it)
         wait1(&bars.q_full[it & 1], (it >> 1) & 1, wd, ERR_WAIT_DRAIN);
-      if (nd > 0) wait1(bars.do_full, (nd - 1) & 1, wd, ERR_WAIT_DRAIN);
+      for (int it = max(0, nd - C::ND); it < nd; ++it)
+        wait1(&bars.do_full[it % C::ND], (it / C::ND) & 1, wd, ERR_WAIT_DRAIN);
     }
   } else if (warp == 9) {
     // ================================================================ MMA issuer
@@ -312,12 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         issue_s(0);
       }
       for (int it = 0; it < n && ok; ++it) {
-        const int s = it & 1;
+        const int s = it & 1, sd = it % C::ND;
         const uint32_t q_a = smem_u32(smem + C::OFF_Q + s * C::TILE);
-        const uint32_t do_a = smem_u32(smem + C::OFF_DO);
-        // dP^T = V dO^T, once dQ of the previous tile has left TMEM
-        if (it > 0 && !(ok = wait1(bars.dq_empty, (it - 1) & 1, wc, ERR_WAIT_MMA))) break;
-        if (!(ok = wait1(bars.do_full, it & 1, wc, ERR_WAIT_MMA))) break;
+        const uint32_t do_a = smem_u32(smem + C::OFF_DO + sd * C::TILE);
+        // dP^T = V dO^T, once dQ of the previous tile has left TMEM (DET: the
+        // dS^T of the previous tile in these columns was read by dK, an
+        // earlier MMA)
+        if (!DET && it > 0 && !(ok = wait1(bars.dq_empty, (it - 1) & 1, wc, ERR_WAIT_MMA))) break;
+        if (!(ok = wait1(&bars.do_full[sd], (it / C::ND) & 1, wc, ERR_WAIT_MMA))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -334,16 +349,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         for (int kk = 0; kk < kT / 16; ++kk)
           mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8,
                  sdesc_sw128(do_a + kk * 2048, C::SUB, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bars.do_empty);   // dV is the last reader of dO(it)
+        mma_commit(&bars.do_empty[sd]);   // dV is the last reader of dO(it)
         if (it + 1 < n) {
           if (!(ok = wait1(&bars.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
             break;
           tc_fence_after();
           issue_s(it + 1);
         }
-        // dK += dS^T Q (A = dS^T: K-major view of the dS boxes) ; dQ = dS K
         if (!(ok = wait1(bars.ds_full, it & 1, wc, ERR_WAIT_MMA))) break;
         tc_fence_after();
+        if (DET) {
+          // dK += dS^T Q with dS^T packed in TMEM like P^T (in the dP^T columns)
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ts(t_dk, t_dp + (kk / 4) * 64 + (kk % 4) * 8,
+                   sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars.q_empty[s]);
+          // the epilogue reads dK and dV once every MMA of the CTA is done
+          if (it == n - 1) mma_commit(bars.dq_full);
+          continue;
+        }
+        // dK += dS^T Q (A = dS^T: K-major view of the dS boxes) ; dQ = dS K
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
           mma_ss(t_dk, sdesc_sw128(ds_a + (kk / 4) * C::SUB + (kk % 4) * 32, 16, 1024),
@@ -482,6 +509,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         dsk[e / 2] = pack_bf16x2(d[0], d[1]);
         dsk[e / 2 + 1] = pack_bf16x2(d[2], d[3]);
       }
+      if (DET) {
+        // into the first half of this warpgroup's own dP^T columns, all of
+        // which it has read above
+        tmem_st16(lane_base + 128 + h * 64, dsk);
+        tmem_st16(lane_base + 128 + h * 64 + 16, dsk + 16);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bars.ds_full);
+        return true;
+      }
       // the staged dQ of the previous tile must have been read by TMA
       if (lane == 0) bulk_wait_group_read0();
       __syncwarp();
@@ -506,10 +543,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     for (; ok && it < n; ++it) {
       if (!(ok = compute_ds(it))) break;
       if (it + 1 < n && !(ok = compute_p(it + 1))) break;
-      if (!(ok = dq_readout(it))) break;   // the last one: every MMA of this CTA is done
+      if (!DET && !(ok = dq_readout(it))) break;   // the last one: every MMA of this CTA is done
     }
-    if (lane == 0) bulk_wait_group0();     // reductions complete before the CTA exits
-    __syncwarp();
+    if (!DET) {
+      if (lane == 0) bulk_wait_group0();   // reductions complete before the CTA exits
+      __syncwarp();
+    } else if (ok && it == n && n > 0) {
+      // (the non-deterministic path waited for this in the last dQ read-out)
+      ok = wait_warp(bars.dq_full, 0, wc, ERR_WAIT_EPILOGUE);
+      tc_fence_after();
+    }
     // ---- dK, dV of this key tile (this warpgroup's half of the columns)
     if (ok && it == n) {
       const bool have = n > 0;
@@ -552,10 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   }
 }
 
-template <int D, bool CAUSAL, bool BIAS>
+template <int D, bool CAUSAL, bool BIAS, bool DET>
 cudaError_t launch_main(const BwdBf16Args& a, cudaStream_t s) {
-  using C = BwdCfg<D>;
-  auto kern = bwd_main_kernel<D, CAUSAL, BIAS>;
+  using C = BwdCfg<D, DET>;
+  auto kern = bwd_main_kernel<D, CAUSAL, BIAS, DET>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
   if (e != cudaSuccess) return e;
   const long BHkv = (long)a.p.B * a.p.Hkv;
@@ -581,11 +624,22 @@ cudaError_t launch_d(const BwdBf16Args& a, cudaStream_t s, unsigned stages) {
   if (stages & BWD_MAIN) {
     const BwdBf16Args& m = a;
     const bool bias = a.bias != nullptr;
-    if (a.p.causal)
-      e = bias ? launch_main<D, true, true>(m, s) : launch_main<D, true, false>(m, s);
-    else
-      e = bias ? launch_main<D, false, true>(m, s) : launch_main<D, false, false>(m, s);
+    if (stages & BWD_DET) {
+      if (a.p.causal)
+        e = bias ? launch_main<D, true, true, true>(m, s) : launch_main<D, true, false, true>(m, s);
+      else
+        e = bias ? launch_main<D, false, true, true>(m, s) : launch_main<D, false, false, true>(m, s);
+    } else {
+      if (a.p.causal)
+        e = bias ? launch_main<D, true, true, false>(m, s) : launch_main<D, true, false, false>(m, s);
+      else
+        e = bias ? launch_main<D, false, true, false>(m, s)
+                 : launch_main<D, false, false, false>(m, s);
+    }
     if (e != cudaSuccess) return e;
+  }
+  if (stages & BWD_DQ) {
+    if ((e = launch_bwd_dq(a, s)) != cudaSuccess) return e;
   }
   if (stages & BWD_POST) {
     const long n4 = rows * D / 4;

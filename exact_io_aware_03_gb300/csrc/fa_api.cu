@@ -291,6 +291,11 @@ size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int max_seqlen_q,
   return bwd_ws_bytes(B, H, max_seqlen_q, (size_t)H * total_q, d);
 }
 
+size_t fa_bwd_deterministic_workspace_size(int B, int H, int Nq, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || d < 1) return 0;
+  return bwd_ws_bytes(B, H, Nq, 0, d);
+}
+
 }  // extern "C"
 
 namespace {
@@ -316,7 +321,8 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
     if (!aligned(ptr, 16)) return FA_ERR_INVALID_ARG;
   if (!aligned(lse, 4) || (key_bias && !aligned(key_bias, 4)) || !aligned(workspace, 256))
     return FA_ERR_INVALID_ARG;
-  const size_t dq_rows = varlen ? (size_t)H * total_q : (size_t)B * H * Nq;
+  const bool det = (stages & fa::BWD_DET) != 0;   // no dQ accumulator
+  const size_t dq_rows = det ? 0 : varlen ? (size_t)H * total_q : (size_t)B * H * Nq;
   if (workspace_bytes < bwd_ws_bytes(B, H, Nq, dq_rows, d)) return FA_ERR_INVALID_ARG;
 
   fa::BwdBf16Args a;
@@ -329,7 +335,7 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   // tensor-map views: (d, rows per head coordinate, head coordinates)
   const int qh = varlen ? H : B * H, kh = varlen ? Hkv : B * Hkv;
   const int qn = varlen ? total_q : Nq, kn = varlen ? total_k : Nk;
-  if (stages & fa::BWD_MAIN) {
+  if (stages & (fa::BWD_MAIN | fa::BWD_DQ)) {
     if ((st = make_map(&a.tm_q, q, qh, qn, d)) != FA_OK) return st;
     if ((st = make_map(&a.tm_k, k, kh, kn, d)) != FA_OK) return st;
     if ((st = make_map(&a.tm_v, v, kh, kn, d)) != FA_OK) return st;
@@ -344,8 +350,9 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   char* ws = static_cast<char*>(workspace);
   a.D = reinterpret_cast<float*>(ws);
   a.lse2 = reinterpret_cast<float*>(ws + round256(prow * 4));
-  a.dq_acc = reinterpret_cast<float*>(ws + 2 * round256(prow * 4));
-  if ((stages & fa::BWD_MAIN) && (st = make_map_f32_acc(&a.tm_dqacc, a.dq_acc, qh, qn, d)) != FA_OK)
+  a.dq_acc = det ? nullptr : reinterpret_cast<float*>(ws + 2 * round256(prow * 4));
+  if (!det && (stages & fa::BWD_MAIN) &&
+      (st = make_map_f32_acc(&a.tm_dqacc, a.dq_acc, qh, qn, d)) != FA_OK)
     return st;
   a.dq = static_cast<uint16_t*>(dq);
   a.dk = static_cast<uint16_t*>(dk);
@@ -421,6 +428,43 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
   return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d, scale,
                     causal, dtype, workspace, workspace_bytes, stream,
                     fa::BWD_PRE | fa::BWD_MAIN | fa::BWD_POST);
+}
+
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                               const float* key_bias, int B, int H, int H_kv, int Nq, int Nk,
+                               int d, float scale, int causal, fa_dtype dtype, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d, scale,
+                    causal, dtype, workspace, workspace_bytes, stream,
+                    fa::BWD_PRE | fa::BWD_MAIN | fa::BWD_DQ | fa::BWD_DET);
+}
+
+fa_status fa_bwd_deterministic_stage(const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dO, void* dq, void* dk,
+                                     void* dv, const float* key_bias, int B, int H, int H_kv,
+                                     int Nq, int Nk, int d, float scale, int causal,
+                                     fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                                     void* stream, int stage) {
+  static const unsigned kStages[3] = {fa::BWD_PRE, fa::BWD_MAIN, fa::BWD_DQ};
+  if (stage < 1 || stage > 3) return FA_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d, scale,
+                    causal, dtype, workspace, workspace_bytes, stream,
+                    kStages[stage - 1] | fa::BWD_DET);
+}
+
+fa_status fa_bwd_varlen_deterministic(const void* q, const void* k, const void* v,
+                                      const void* o, const float* lse, const void* dO, void* dq,
+                                      void* dk, void* dv, const int* cu_seqlens_q,
+                                      const int* cu_seqlens_k, int B, int H, int H_kv,
+                                      int total_q, int total_k, int max_seqlen_q,
+                                      int max_seqlen_k, int d, float scale, int causal,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!cu_seqlens_q) return FA_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, nullptr, B, H, H_kv, max_seqlen_q,
+                    max_seqlen_k, d, scale, causal, FA_DTYPE_BF16, workspace, workspace_bytes,
+                    stream, fa::BWD_PRE | fa::BWD_MAIN | fa::BWD_DQ | fa::BWD_DET, cu_seqlens_q,
+                    cu_seqlens_k, total_q, total_k);
 }
 
 fa_status fa_selftest_device_timeout(void* stream) {

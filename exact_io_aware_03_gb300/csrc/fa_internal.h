@@ -98,13 +98,17 @@ struct BwdBf16Args {
   uint32_t* err;
   int num_sms;
   int nq_pad;          // Nq rounded up to a multiple of 128
+  int head_group;      // dQ kernel: heads per CTA-ordering group (set by its launcher)
 };
 
 cudaError_t launch_fwd_f32(const FwdF32Args& a, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const FwdBf16Args& a, cudaStream_t s);
 // Backward stages (bit mask): D / base-2 LSE / zeroed dQ accumulator; the
-// tensor-core main loop; the dQ conversion.
-enum : unsigned { BWD_PRE = 1u, BWD_MAIN = 2u, BWD_POST = 4u };
+// tensor-core main loop; the dQ conversion. BWD_DET selects the deterministic
+// variant of the main loop (dK, dV only; no accumulator is zeroed when dq_acc
+// is null) and BWD_DQ the query-outer dQ kernel that completes it.
+enum : unsigned { BWD_PRE = 1u, BWD_MAIN = 2u, BWD_POST = 4u, BWD_DET = 8u, BWD_DQ = 16u };
 cudaError_t launch_bwd_bf16(const BwdBf16Args& a, cudaStream_t s, unsigned stages);
+cudaError_t launch_bwd_dq(const BwdBf16Args& a, cudaStream_t s);
 
 }  // namespace fa

@@ -214,6 +214,45 @@ fa_status fa_bwd_postprocess(const void *q, const void *k, const void *v, const 
                              void *stream);
 
 /*
+ * Deterministic backward ("flash-attention", Part VII: the backward's
+ * deterministic option). fa_bwd accumulates dQ over key tiles with
+ * reductions whose order depends on timing, so dq may differ in the last
+ * bits between runs. Here dq is formed by a second, query-tile-outer kernel
+ * that adds the key tiles' contributions in a fixed order inside one CTA, so
+ * dq, dk and dv are bitwise identical from run to run for the same inputs
+ * and device. Same arguments and results as fa_bwd_gqa (H_kv == H: plain
+ * multi-head) and fa_bwd_varlen respectively. S and P are recomputed in both
+ * kernels (seven tile products per (query tile, key tile) pair instead of
+ * five); no dQ accumulator is needed, so the workspace is only D and the
+ * base-2 LSE: fa_bwd_deterministic_workspace_size(B, H, Nq, d) bytes (for
+ * the varlen call: Nq = max_seqlen_q), 256-byte aligned, contents on entry
+ * irrelevant.
+ * fa_bwd_deterministic_stage runs one of its three launches (stage 1:
+ * preprocess; 2: dK and dV; 3: dQ); in that order on one stream they equal
+ * fa_bwd_deterministic. Invalid stage numbers give FA_ERR_INVALID_ARG.
+ */
+size_t fa_bwd_deterministic_workspace_size(int B, int H, int Nq, int d);
+fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
+                               const float *lse, const void *dO,
+                               void *dq, void *dk, void *dv, const float *key_bias,
+                               int B, int H, int H_kv, int Nq, int Nk, int d, float scale,
+                               int causal, fa_dtype dtype, void *workspace,
+                               size_t workspace_bytes, void *stream);
+fa_status fa_bwd_deterministic_stage(const void *q, const void *k, const void *v, const void *o,
+                                     const float *lse, const void *dO,
+                                     void *dq, void *dk, void *dv, const float *key_bias,
+                                     int B, int H, int H_kv, int Nq, int Nk, int d, float scale,
+                                     int causal, fa_dtype dtype, void *workspace,
+                                     size_t workspace_bytes, void *stream, int stage);
+fa_status fa_bwd_varlen_deterministic(const void *q, const void *k, const void *v, const void *o,
+                                      const float *lse, const void *dO, void *dq, void *dk,
+                                      void *dv, const int *cu_seqlens_q, const int *cu_seqlens_k,
+                                      int B, int H, int H_kv, int total_q, int total_k,
+                                      int max_seqlen_q, int max_seqlen_k, int d, float scale,
+                                      int causal, void *workspace, size_t workspace_bytes,
+                                      void *stream);
+
+/*
  * Size in bytes of the device array fa_bwd_noalloc uses as its workspace.
  */
 #define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)

@@ -147,3 +147,26 @@ def test_gqa_rejects_bad_head_counts(lib, H, H_kv):
              key_bias=None, B=1, H=H, H_kv=H_kv, Nq=16, Nk=16, d=64, scale=0.125, causal=1,
              dtype=fa.FA_DTYPE_BF16, workspace=FAKE, workspace_bytes=1 << 20, stream=None)
     assert fa.fa_bwd_gqa(**b) == fa.FA_ERR_INVALID_ARG
+
+
+def test_deterministic_backward_workspace_and_validation(lib):
+    B, H, Nq, d = 2, 3, 129, 128
+    r256 = lambda x: (x + 255) // 256 * 256
+    # only D and the base-2 LSE, 128-row padded per head: no dQ accumulator
+    assert fa.fa_bwd_deterministic_workspace_size(B, H, Nq, d) == 2 * r256(B * H * 256 * 4)
+    assert fa.fa_bwd_deterministic_workspace_size(0, H, Nq, d) == 0
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dO=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             key_bias=None, B=B, H=H, H_kv=H, Nq=Nq, Nk=300, d=d, scale=0.1, causal=1,
+             dtype=fa.FA_DTYPE_BF16, workspace=FAKE,
+             workspace_bytes=fa.fa_bwd_deterministic_workspace_size(B, H, Nq, d) - 1,
+             stream=None)
+    assert fa.fa_bwd_deterministic(**a) == fa.FA_ERR_INVALID_ARG       # workspace too small
+    for bad, expect in ((dict(d=96), fa.FA_ERR_UNSUPPORTED), (dict(H_kv=2), fa.FA_ERR_INVALID_ARG),
+                        (dict(workspace=FAKE + 64), fa.FA_ERR_INVALID_ARG),
+                        (dict(dtype=fa.FA_DTYPE_FP32), fa.FA_ERR_UNSUPPORTED)):
+        b = dict(a, workspace_bytes=1 << 30)
+        b.update(bad)
+        assert fa.fa_bwd_deterministic(**b) == expect, bad
+    for stage in (0, 4, -1):
+        assert fa.fa_bwd_deterministic_stage(**dict(a, workspace_bytes=1 << 30),
+                                             stage=stage) == fa.FA_ERR_INVALID_ARG

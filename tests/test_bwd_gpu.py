@@ -27,17 +27,19 @@ def built():
     torch.cuda.init()
 
 
-def run_fwd_bwd(q, k, v, dO, bias, causal, scale):
+def run_fwd_bwd(q, k, v, dO, bias, causal, scale, deterministic=False):
     dev = "cuda"
     qd, kd, vd, dOd = (t.to(dev) for t in (q, k, v, dO))
     bd = None if bias is None else bias.to(dev)
     o, lse = fa.fwd(qd, kd, vd, key_bias=bd, causal=causal, scale=scale)
     gq, gk, gv = Guarded(q.shape, q.dtype), Guarded(k.shape, k.dtype), Guarded(v.shape, v.dtype)
-    ws_bytes = fa.fa_bwd_workspace_size(*q.shape[:3], k.shape[2], q.shape[3])
+    B, H, Nq, d = q.shape
+    ws_bytes = (fa.fa_bwd_deterministic_workspace_size(B, H, Nq, d) if deterministic
+                else fa.fa_bwd_workspace_size(B, H, Nq, k.shape[2], d))
     ws = Guarded((ws_bytes,), torch.uint8)
     ws.t.fill_(0x7f)   # stale contents must not matter
     fa.bwd(qd, kd, vd, o, lse, dOd, key_bias=bd, causal=causal, scale=scale, workspace=ws.t,
-           dq=gq.t, dk=gk.t, dv=gv.t)
+           dq=gq.t, dk=gk.t, dv=gv.t, deterministic=deterministic)
     fa.check_device_error()
     for g, nm in ((gq, "dQ"), (gk, "dK"), (gv, "dV"), (ws, "workspace")):
         g.check(nm)

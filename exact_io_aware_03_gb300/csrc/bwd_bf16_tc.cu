@@ -39,6 +39,7 @@
 // dS^T goes to shared memory only: it is the A operand of both dK (K-major
 // view) and dQ (MN-major view), so the S^T columns are free as soon as dV has
 // read P^T, and S^T of the next tile overlaps dK and dQ of this one.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -182,15 +183,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   int* any_key = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 8);
   const WaitCtx wc{abort_flag, a.err};
 
-  // Head-major order: the CTAs running together cover few heads, so their Q,
-  // dO and dQ accumulator stay in L2; within a head the low key tiles (the
-  // most query tiles under a causal mask) come first.
   // One CTA per (key/value head, key tile). With grouped heads it walks the
   // query tiles of every query head of its group, so dK and dV of the shared
   // head accumulate over the whole group in TMEM.
+  // Order: heads in groups of a.head_group whose Q, dO (and dQ accumulator)
+  // stay in L2 together; within a group, key tile by key tile over the
+  // group's heads, low key tiles (the most query tiles under a causal mask)
+  // first, so that the last CTAs to start are the short ones.
   const int n_kt = (p.Nk + kT - 1) / kT;
-  const int bh_kv = (int)(blockIdx.x / n_kt);
-  const int jt = (int)(blockIdx.x % n_kt);
+  const int BHkv = p.B * p.Hkv;
+  const int G = a.head_group;
+  const int grp_i = (int)(blockIdx.x / ((long)G * n_kt));
+  const int g0 = grp_i * G;
+  const int gsz = min(G, BHkv - g0);
+  const int rr = (int)(blockIdx.x - (long)g0 * n_kt);
+  const int bh_kv = g0 + rr % gsz;
+  const int jt = rr / gsz;
   const int b = bh_kv / p.Hkv;
   const int grp = p.H / p.Hkv;
   const int h_q0 = (bh_kv % p.Hkv) * grp;   // first query head of the group
@@ -341,24 +349,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
                  kk > 0);
         }
         mma_commit(bars.dp_full);
+        // dV(it) and S(it+1) are issued back to back once both can go: a wait
+        // between two products would let the MMA queue run dry
+        if (!(ok = wait1(bars.p_full, it & 1, wc, ERR_WAIT_MMA))) break;
+        if (it + 1 < n &&
+            !(ok = wait1(&bars.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
+          break;
+        tc_fence_after();
         // dV += P^T dO  (P^T packed bf16: query columns [0,64) in TMEM columns
         // [0,32), [64,128) in [64,96))
-        if (!(ok = wait1(bars.p_full, it & 1, wc, ERR_WAIT_MMA))) break;
-        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
           mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8,
                  sdesc_sw128(do_a + kk * 2048, C::SUB, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.do_empty[sd]);   // dV is the last reader of dO(it)
-        if (it + 1 < n) {
-          if (!(ok = wait1(&bars.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
-            break;
-          tc_fence_after();
-          issue_s(it + 1);
-        }
+        if (it + 1 < n) issue_s(it + 1);
         if (!(ok = wait1(bars.ds_full, it & 1, wc, ERR_WAIT_MMA))) break;
         tc_fence_after();
-        if (DET) {
+        if constexpr (DET) {
           // dK += dS^T Q with dS^T packed in TMEM like P^T (in the dP^T columns)
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk)
@@ -368,19 +376,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           mma_commit(&bars.q_empty[s]);
           // the epilogue reads dK and dV once every MMA of the CTA is done
           if (it == n - 1) mma_commit(bars.dq_full);
-          continue;
+        } else {
+          // dK += dS^T Q (A = dS^T: K-major view of the dS boxes) ; dQ = dS K
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ss(t_dk, sdesc_sw128(ds_a + (kk / 4) * C::SUB + (kk % 4) * 32, 16, 1024),
+                   sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ss(t_dp, sdesc_sw128(ds_a + kk * 2048, C::SUB, 1024),
+                   sdesc_sw128(k_a + kk * 2048, C::SUB, 1024), id_dq, kk > 0 ? 1u : 0u);
+          mma_commit(bars.dq_full);
+          mma_commit(&bars.q_empty[s]);
         }
-        // dK += dS^T Q (A = dS^T: K-major view of the dS boxes) ; dQ = dS K
-#pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ss(t_dk, sdesc_sw128(ds_a + (kk / 4) * C::SUB + (kk % 4) * 32, 16, 1024),
-                 sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ss(t_dp, sdesc_sw128(ds_a + kk * 2048, C::SUB, 1024),
-                 sdesc_sw128(k_a + kk * 2048, C::SUB, 1024), id_dq, kk > 0 ? 1u : 0u);
-        mma_commit(bars.dq_full);
-        mma_commit(&bars.q_empty[s]);
       }
       mma_commit(bars.drain);
       wait1(bars.drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
@@ -473,11 +482,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           P[e + j] = ex2(x[j]);
         }
       }
-      uint32_t pk[32];
 #pragma unroll
-      for (int e = 0; e < 64; e += 2) pk[e / 2] = pack_bf16x2(P[e], P[e + 1]);
-      tmem_st16(lane_base + h * 64, pk);
-      tmem_st16(lane_base + h * 64 + 16, pk + 16);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          pk[e / 2] = pack_bf16x2(P[half * 32 + e], P[half * 32 + e + 1]);
+        tmem_st16(lane_base + h * 64 + half * 16, pk);
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bars.p_full);
@@ -489,48 +501,55 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       const float* std_ = stat + (it & 1) * 2 * kT + kT + h * 64;
       if (!wait_warp(bars.dp_full, it & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
-      uint32_t dpv[64];
-      tmem_ld32(lane_base + 128 + h * 64, dpv);
-      tmem_ld32(lane_base + 128 + h * 64 + 32, dpv + 32);
-      tmem_ld_wait();
-      uint32_t dsk[32];
+      // two chunks of 32 query columns, to keep the live registers low
 #pragma unroll
-      for (int e = 0; e < 64; e += 4) {
-        const float4 D4 = *reinterpret_cast<const float4*>(std_ + e);
-        float d[4];
-        f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
-                            f2_pack(D4.x, D4.y)),
-                       f2_pack(P[e], P[e + 1])),
-                  d[0], d[1]);
-        f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
-                            f2_pack(D4.z, D4.w)),
-                       f2_pack(P[e + 2], P[e + 3])),
-                  d[2], d[3]);
-        dsk[e / 2] = pack_bf16x2(d[0], d[1]);
-        dsk[e / 2 + 1] = pack_bf16x2(d[2], d[3]);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t dpv[32];
+        tmem_ld32(lane_base + 128 + h * 64 + half * 32, dpv);
+        tmem_ld_wait();
+        uint32_t dsk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 D4 = *reinterpret_cast<const float4*>(std_ + half * 32 + e);
+          const float* Pp = P + half * 32 + e;
+          float d[4];
+          f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                              f2_pack(D4.x, D4.y)),
+                         f2_pack(Pp[0], Pp[1])),
+                    d[0], d[1]);
+          f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
+                              f2_pack(D4.z, D4.w)),
+                         f2_pack(Pp[2], Pp[3])),
+                    d[2], d[3]);
+          dsk[e / 2] = pack_bf16x2(d[0], d[1]);
+          dsk[e / 2 + 1] = pack_bf16x2(d[2], d[3]);
+        }
+        if (DET) {
+          // packed into this warpgroup's own dP^T columns, over scores it has
+          // already read (chunk 0 -> columns [0,16), chunk 1 -> [16,32))
+          tmem_st16(lane_base + 128 + h * 64 + half * 16, dsk);
+        } else {
+          if (half == 0) {
+            // the staged dQ of the previous tile must have been read by TMA
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+          }
+          // row = key of the 128-byte-swizzled box holding query columns
+          // [64h, 64h+64); this chunk is its 16-byte pieces 4*half .. 4*half+3
+          uint8_t* rowp = ds_s + h * C::SUB + r * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int chunk = (half * 4 + k) ^ (r & 7);
+            *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+                make_uint4(dsk[4 * k], dsk[4 * k + 1], dsk[4 * k + 2], dsk[4 * k + 3]);
+          }
+        }
       }
       if (DET) {
-        // into the first half of this warpgroup's own dP^T columns, all of
-        // which it has read above
-        tmem_st16(lane_base + 128 + h * 64, dsk);
-        tmem_st16(lane_base + 128 + h * 64 + 16, dsk + 16);
         tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bars.ds_full);
-        return true;
+      } else {
+        fence_proxy_async_smem();
       }
-      // the staged dQ of the previous tile must have been read by TMA
-      if (lane == 0) bulk_wait_group_read0();
-      __syncwarp();
-      // row = key of the 128-byte-swizzled box holding query columns [64h, 64h+64)
-      uint8_t* rowp = ds_s + h * C::SUB + r * 128;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int chunk = k ^ (r & 7);
-        *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-            make_uint4(dsk[4 * k], dsk[4 * k + 1], dsk[4 * k + 2], dsk[4 * k + 3]);
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bars.ds_full);
       return true;
@@ -603,7 +622,12 @@ cudaError_t launch_main(const BwdBf16Args& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const long BHkv = (long)a.p.B * a.p.Hkv;
   const long n_kt = (a.p.Nk + kT - 1) / kT;
-  kern<<<(unsigned)(BHkv * n_kt), kThreads, C::BYTES, s>>>(a);
+  // heads per ordering group: the Q and dO every CTA of a key/value head
+  // streams (all query heads of its group) within ~48 MiB of L2
+  const long q_bytes = 2L * (a.p.H / a.p.Hkv) * a.p.Nq * D * 2;
+  BwdBf16Args b = a;
+  b.head_group = (int)std::max(1L, std::min(BHkv, (48L << 20) / std::max(q_bytes, 1L)));
+  kern<<<(unsigned)(BHkv * n_kt), kThreads, C::BYTES, s>>>(b);
   return cudaGetLastError();
 }
 

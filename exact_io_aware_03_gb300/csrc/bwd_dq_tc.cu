@@ -21,10 +21,13 @@
 // Warp roles (320 threads, one CTA per SM): warps 0-7 are two warpgroups that
 // split the 128 keys of every tile (thread = query row = TMEM lane, warpgroup
 // h takes keys [64h, 64h+64)); warp 8 issues the TMA loads; warp 9 owns TMEM
-// and issues the MMAs. TMEM (512 columns): S of even / odd key tiles [0,128)
-// and [128,256) (so S of tile j+1 is computed while tile j is exponentiated),
-// dP then packed dS [256,384), dQ [384, 384+D).
-// MMA order per key tile j: dP(j), S(j+1), then dQ(j) once dS(j) is in TMEM.
+// and issues the MMAs. Q_i and dO_i are copied once from shared memory into
+// TMEM, so that all three products read their A operand from TMEM (the
+// shared-memory operand path is the slower one: it has to stream both
+// operands). TMEM (512 columns): S [0,128), dP then packed dS [128,256),
+// dQ [256,256+D), Q_i [256+D, 256+3D/2), dO_i [256+3D/2, 256+2D) (bf16 pairs).
+// MMA order per key tile j: dP(j), S(j+1) (once the warpgroups have read
+// S(j)), then dQ(j) once dS(j) is in TMEM.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -39,42 +42,49 @@ constexpr int kThreads = 320;
 constexpr int kT = 128;   // query rows per tile = keys per key tile
 constexpr float kLog2e = 1.4426950408889634f;
 
+// K_j is read twice, by S(j) and, a tile later, by dQ(j), so the K ring has
+// one stage more than the V ring (V_j is read by dP(j) only): the load of
+// K_{j+1} then starts a whole tile before S(j+1) needs it instead of when
+// dQ(j-1) completes, which left the tensor core waiting for the copy.
 template <int D>
 struct DqCfg {
-  static constexpr int NS = (D == 128) ? 2 : 4;   // K/V ring stages
+  static constexpr int NSK = (D == 128) ? 3 : 4;  // K ring stages
+  static constexpr int NSV = (D == 128) ? 2 : 4;  // V ring stages
   static constexpr int TILE = kT * D * 2;         // bf16 [128][D]
   static constexpr int SUB = kT * 128;            // one 64-column box
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = TILE;
   static constexpr int OFF_K = 2 * TILE;
-  static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_BIAS = OFF_V + NS * TILE;   // [2 warpgroups][2 bufs][128] floats
+  static constexpr int OFF_V = OFF_K + NSK * TILE;
+  static constexpr int OFF_BIAS = OFF_V + NSV * TILE;   // [2 warpgroups][2 bufs][128] floats
   static constexpr int OFF_BAR = OFF_BIAS + 2 * 2 * kT * 4;
-  static constexpr int NBAR = 1 /*q_full*/ + 4 * NS /*k/v full/empty*/ + 2 /*s_full*/ +
-                              1 /*dp_full*/ + 1 /*ds_full*/ + 1 /*dq_full*/ + 4 /*bias*/ +
-                              1 /*drain*/;
+  static constexpr int NBAR = 1 /*q_full*/ + 2 * NSK + 2 * NSV /*k/v full/empty*/ +
+                              1 /*s_full*/ + 1 /*s_free*/ + 1 /*dp_full*/ + 1 /*ds_full*/ +
+                              1 /*dq_full*/ + 1 /*qt_ready*/ + 4 /*bias*/ + 1 /*drain*/;
   static constexpr int OFF_SCALARS = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_SCALARS + 64;
-  static constexpr int SMEM_ALLOC = BYTES + 1024;   // slack for 1024-byte alignment
 };
 
 template <int D, bool CAUSAL, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdBf16Args a) {
   using C = DqCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 128-byte-swizzled TMA boxes need 1024-byte alignment; the dynamic
+  // shared memory of a kernel without static shared memory starts there
+  // (checked below: a misaligned base aborts the CTA with an error)
+  extern __shared__ __align__(1024) uint8_t smem[];
   const Problem& p = a.p;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
 
   uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bb;   bb += 1;   // Q_i and dO_i
-  uint64_t* k_full = bb;   bb += C::NS;
-  uint64_t* k_empty = bb;  bb += C::NS;
-  uint64_t* v_full = bb;   bb += C::NS;
-  uint64_t* v_empty = bb;  bb += C::NS;
-  uint64_t* s_full = bb;   bb += 2;   // S of even / odd key tiles done
+  uint64_t* k_full = bb;   bb += C::NSK;
+  uint64_t* k_empty = bb;  bb += C::NSK;
+  uint64_t* v_full = bb;   bb += C::NSV;
+  uint64_t* v_empty = bb;  bb += C::NSV;
+  uint64_t* s_full = bb;   bb += 1;   // S done
+  uint64_t* s_free = bb;   bb += 1;   // S read by both warpgroups (256 arrivals)
+  uint64_t* qt_ready = bb; bb += 1;   // Q_i, dO_i copied into TMEM (256 arrivals)
   uint64_t* dp_full = bb;  bb += 1;
   uint64_t* ds_full = bb;  bb += 1;   // dS in TMEM (256 arrivals)
   uint64_t* dq_full = bb;  bb += 1;   // every dQ product done
@@ -106,21 +116,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   const float* bias_row = BIAS ? a.bias + (size_t)b * Nk : nullptr;
 
   if (threadIdx.x == 0) {
+    if ((smem_u32(smem) & 1023u) != 0) atomicOr(a.err, ERR_WAIT_DRAIN);   // layout invariant
     mbar_init(q_full, 1);
-    for (int s = 0; s < C::NS; ++s) {
+    for (int s = 0; s < C::NSK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < C::NSV; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 2 * kT);
+    mbar_init(qt_ready, 2 * kT);
     mbar_init(dp_full, 1);
     mbar_init(ds_full, 2 * kT);
     mbar_init(dq_full, 1);
     for (int t = 0; t < 4; ++t) mbar_init(&bias_rdy[t], kT);
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    *abort_flag = (smem_u32(smem) & 1023u) != 0;
     *key_lo_s = Nk;
     *key_hi_s = -1;
     fence_mbar_init();
@@ -173,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     hi = lim < 0 ? 0 : (int)min((long)hi, lim / kT + 1);
   }
   hi = max(hi, lo);
-  const int n = hi - lo;
+  const int n = *abort_flag ? 0 : hi - lo;
 
   if (warp == 8) {
     // ================================================================ TMA producer
@@ -185,69 +199,75 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       }
       int nk = 0, nv = 0;
       for (int j = lo; j < hi; ++j) {
-        const int i = j - lo, s = i % C::NS, u = i / C::NS;
-        if (u > 0 && !wait1(&k_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
-        mbar_arrive_expect_tx(&k_full[s], C::TILE);
+        const int i = j - lo;
+        const int sk = i % C::NSK, uk = i / C::NSK, sv_ = i % C::NSV, uv = i / C::NSV;
+        if (uk > 0 && !wait1(&k_empty[sk], (uk - 1) & 1, wc, ERR_WAIT_LOAD)) break;
+        mbar_arrive_expect_tx(&k_full[sk], C::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::SUB, &a.tm_k, c * 64,
-                      sv.k_off + j * kT, sv.hk, &k_full[s]);
+          tma_load_3d(smem + C::OFF_K + sk * C::TILE + c * C::SUB, &a.tm_k, c * 64,
+                      sv.k_off + j * kT, sv.hk, &k_full[sk]);
         ++nk;
-        if (u > 0 && !wait1(&v_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
-        mbar_arrive_expect_tx(&v_full[s], C::TILE);
+        if (uv > 0 && !wait1(&v_empty[sv_], (uv - 1) & 1, wc, ERR_WAIT_LOAD)) break;
+        mbar_arrive_expect_tx(&v_full[sv_], C::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::SUB, &a.tm_v, c * 64,
-                      sv.k_off + j * kT, sv.hk, &v_full[s]);
+          tma_load_3d(smem + C::OFF_V + sv_ * C::TILE + c * C::SUB, &a.tm_v, c * 64,
+                      sv.k_off + j * kT, sv.hk, &v_full[sv_]);
         ++nv;
       }
       // no copy may still be landing when the CTA exits (bounded, ignores abort)
       const WaitCtx wd{abort_flag, a.err, true};
       wait1(q_full, 0, wd, ERR_WAIT_DRAIN);
-      for (int i = max(0, nk - C::NS); i < nk; ++i)
-        wait1(&k_full[i % C::NS], (i / C::NS) & 1, wd, ERR_WAIT_DRAIN);
-      for (int i = max(0, nv - C::NS); i < nv; ++i)
-        wait1(&v_full[i % C::NS], (i / C::NS) & 1, wd, ERR_WAIT_DRAIN);
+      for (int i = max(0, nk - C::NSK); i < nk; ++i)
+        wait1(&k_full[i % C::NSK], (i / C::NSK) & 1, wd, ERR_WAIT_DRAIN);
+      for (int i = max(0, nv - C::NSV); i < nv; ++i)
+        wait1(&v_full[i % C::NSV], (i / C::NSV) & 1, wd, ERR_WAIT_DRAIN);
     }
   } else if (warp == 9) {
     // ================================================================ MMA issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);   // S, dP (K-major)
       constexpr uint32_t id_dq = idesc_bf16_f32(kT, D, false, true);    // dQ: B = K, MN-major
-      const uint32_t q_a = smem_u32(smem + C::OFF_Q), do_a = smem_u32(smem + C::OFF_DO);
       const uint32_t k_a = smem_u32(smem + C::OFF_K), v_a = smem_u32(smem + C::OFF_V);
-      const uint32_t t_dp = tmem + 256, t_dq = tmem + 384;
-      // D = A B^T over the head dimension, both operands K-major 64-column boxes
-      auto issue_nt = [&](uint32_t d, uint32_t a_s, uint32_t b_s) {
+      const uint32_t t_s = tmem, t_dp = tmem + 128, t_dq = tmem + 256;
+      const uint32_t t_q = tmem + 256 + D, t_do = tmem + 256 + D + D / 2;
+      // D = A B^T over the head dimension: A (Q or dO) in TMEM, B (K or V) a
+      // K-major tile of 64-column boxes
+      auto issue_nt = [&](uint32_t d, uint32_t a_t, uint32_t b_s) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
-          mma_ss(d, sdesc_sw128(a_s + o, 16, 1024), sdesc_sw128(b_s + o, 16, 1024), id_s, kk > 0);
+          mma_ts(d, a_t + kk * 8, sdesc_sw128(b_s + o, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = wait1(q_full, 0, wc, ERR_WAIT_MMA) && wait1(&k_full[0], 0, wc, ERR_WAIT_MMA);
+      bool ok = wait1(qt_ready, 0, wc, ERR_WAIT_MMA) && wait1(&k_full[0], 0, wc, ERR_WAIT_MMA);
       if (ok) {
         tc_fence_after();
-        issue_nt(tmem, q_a, k_a);
-        mma_commit(&s_full[0]);
+        issue_nt(t_s, t_q, k_a);
+        mma_commit(s_full);
       }
+      // Every wait of an iteration but the one for dS(i) comes first, while
+      // dQ(i-1) is still executing, and dP(i), S(i+1) are then issued back to
+      // back: the issuing thread stalls while the MMA queue is full, so a wait
+      // between two products would leave the tensor core idle.
       for (int i = 0; i < n && ok; ++i) {
-        const int s = i % C::NS;
+        const int s = i % C::NSK, sv_ = i % C::NSV, s1 = (i + 1) % C::NSK;
+        const bool next = i + 1 < n;
+        if (!(ok = wait1(&v_full[sv_], (i / C::NSV) & 1, wc, ERR_WAIT_MMA))) break;
+        // S(i+1) needs K_{i+1} and both warpgroups done reading S(i)
+        if (next && !(ok = wait1(&k_full[s1], ((i + 1) / C::NSK) & 1, wc, ERR_WAIT_MMA))) break;
+        if (next && !(ok = wait1(s_free, i & 1, wc, ERR_WAIT_MMA))) break;
+        tc_fence_after();
         // dP = dO V^T (the dP columns are free: dQ(i-1), which read dS(i-1)
         // there, was issued before and MMAs complete in order)
-        if (!(ok = wait1(&v_full[s], (i / C::NS) & 1, wc, ERR_WAIT_MMA))) break;
-        tc_fence_after();
-        issue_nt(t_dp, do_a, v_a + s * C::TILE);
+        issue_nt(t_dp, t_do, v_a + sv_ * C::TILE);
         mma_commit(dp_full);
-        // S of the next key tile into the other S buffer (its previous scores
-        // were consumed before dS(i-1) was signalled)
-        if (i + 1 < n) {
-          const int s1 = (i + 1) % C::NS;
-          if (!(ok = wait1(&k_full[s1], ((i + 1) / C::NS) & 1, wc, ERR_WAIT_MMA))) break;
-          tc_fence_after();
-          issue_nt(tmem + ((i + 1) & 1) * 128, q_a, k_a + s1 * C::TILE);
-          mma_commit(&s_full[(i + 1) & 1]);
+        mma_commit(&v_empty[sv_]);
+        if (next) {
+          issue_nt(t_s, t_q, k_a + s1 * C::TILE);
+          mma_commit(s_full);
         }
-        // dQ += dS K_j: dS packed bf16, keys [0,64) in TMEM columns [256,288),
-        // keys [64,128) in [320,352)
+        // dQ += dS K_j: dS packed bf16, keys [0,64) in TMEM columns [128,160),
+        // keys [64,128) in [192,224)
         if (!(ok = wait1(ds_full, i & 1, wc, ERR_WAIT_MMA))) break;
         tc_fence_after();
 #pragma unroll
@@ -256,7 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                  sdesc_sw128(k_a + s * C::TILE + kk * 2048, C::SUB, 1024), id_dq,
                  (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&k_empty[s]);
-        mma_commit(&v_empty[s]);
       }
       if (ok) mma_commit(dq_full);
       mma_commit(drain);
@@ -276,6 +295,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     // last visible key of this row / of the tile's first row
     const long lim_row = CAUSAL ? min((long)row + off, (long)Nk - 1) : (long)Nk - 1;
     const long lim_tile = CAUSAL ? min((long)q0 + off, (long)Nk - 1) : (long)Nk - 1;
+    // Q_i and dO_i into TMEM: this thread's row, the warpgroup's half of the
+    // head dimension, read from the 128-byte-swizzled boxes
+    auto copy_q_do = [&]() -> bool {
+      if (!wait_warp(q_full, 0, wc, ERR_WAIT_SOFTMAX)) return false;
+      constexpr int NC = D / 16;                   // 16-byte chunks per half row
+      const int col0 = h * (D / 2);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint8_t* rowp = smem + (which ? C::OFF_DO : C::OFF_Q) + (col0 / 64) * C::SUB + r * 128;
+        uint32_t x[D / 4];
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          const int chunk = ((col0 % 64) / 8 + j) ^ (r & 7);
+          const uint4 u = *reinterpret_cast<const uint4*>(rowp + chunk * 16);
+          x[4 * j] = u.x; x[4 * j + 1] = u.y; x[4 * j + 2] = u.z; x[4 * j + 3] = u.w;
+        }
+        const uint32_t dst = lane_base + 256 + D + which * (D / 2) + h * (D / 4);
+        if constexpr (D == 128) tmem_st32(dst, x);
+        else tmem_st16(dst, x);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(qt_ready);
+      return true;
+    };
     float P[64];
     auto compute_p = [&](int i) -> bool {
       const int key0 = (lo + i) * kT;
@@ -287,12 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         if (!wait_warp(&bias_rdy[h * 2 + (i & 1)], (i >> 1) & 1, wc, ERR_WAIT_SOFTMAX))
           return false;
       }
-      if (!wait_warp(&s_full[i & 1], (i >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) return false;
+      if (!wait_warp(s_full, i & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
       uint32_t* su = reinterpret_cast<uint32_t*>(P);
-      tmem_ld32(lane_base + (i & 1) * 128 + h * 64, su);
-      tmem_ld32(lane_base + (i & 1) * 128 + h * 64 + 32, su + 32);
+      tmem_ld32(lane_base + h * 64, su);
+      tmem_ld32(lane_base + h * 64 + 32, su + 32);
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(s_free);   // the S columns may take the next tile's scores
       const bool need_mask = (long)key0 + kT - 1 > lim_tile;
       const long lim_rel = lim_row - key0 - h * 64;   // local column > lim_rel -> masked
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
@@ -315,30 +361,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     auto compute_ds = [&](int i) -> bool {
       if (!wait_warp(dp_full, i & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
-      uint32_t dpv[64];
-      tmem_ld32(lane_base + 256 + h * 64, dpv);
-      tmem_ld32(lane_base + 256 + h * 64 + 32, dpv + 32);
-      tmem_ld_wait();
       const uint64_t D2 = f2_pack(Drow, Drow);
-      uint32_t pk[32];
+      // two chunks of 32 keys; the packed dS of chunk c goes to columns
+      // [16c, 16c+16) of this warpgroup's own dP columns, already read
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float d0, d1;
-        f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), D2),
-                       f2_pack(P[c], P[c + 1])),
-                  d0, d1);
-        pk[c / 2] = pack_bf16x2(d0, d1);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t dpv[32];
+        tmem_ld32(lane_base + 128 + h * 64 + half * 32, dpv);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float d0, d1;
+          f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), D2),
+                         f2_pack(P[half * 32 + c], P[half * 32 + c + 1])),
+                    d0, d1);
+          pk[c / 2] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(lane_base + 128 + h * 64 + half * 16, pk);
       }
-      // packed into the first half of this warpgroup's own dP columns, all of
-      // which it has already read
-      tmem_st16(lane_base + 256 + h * 64, pk);
-      tmem_st16(lane_base + 256 + h * 64 + 16, pk + 16);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(ds_full);
       return true;
     };
-    bool ok = n == 0 || compute_p(0);
+    bool ok = n == 0 || (copy_q_do() && compute_p(0));
     int i = 0;
     for (; ok && i < n; ++i) {
       if (!(ok = compute_ds(i))) break;
@@ -359,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         for (int c0 = 0; c0 < HD; c0 += 32) {
           uint32_t x[32];
           if (have) {
-            tmem_ld32(lane_base + 384 + h * HD + c0, x);
+            tmem_ld32(lane_base + 256 + h * HD + c0, x);
             tmem_ld_wait();
           } else {
 #pragma unroll
@@ -393,9 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 template <int D, bool CAUSAL, bool BIAS>
 cudaError_t launch_one(const BwdBf16Args& a, cudaStream_t s) {
   using C = DqCfg<D>;
+  static_assert(C::BYTES <= 232448, "shared memory per CTA");
   auto kern = bwd_dq_kernel<D, CAUSAL, BIAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_ALLOC);
+                                       C::BYTES);
   if (e != cudaSuccess) return e;
   const long BH = (long)a.p.B * a.p.H;
   const long n_qt = (a.p.Nq + kT - 1) / kT;
@@ -404,7 +452,7 @@ cudaError_t launch_one(const BwdBf16Args& a, cudaStream_t s) {
   const long kv_bytes = 2L * a.p.Nk * D * 2;
   BwdBf16Args b = a;
   b.head_group = (int)std::max(1L, std::min(BH, (48L << 20) / std::max(kv_bytes, 1L)));
-  kern<<<(unsigned)(BH * n_qt), kThreads, C::SMEM_ALLOC, s>>>(b);
+  kern<<<(unsigned)(BH * n_qt), kThreads, C::BYTES, s>>>(b);
   return cudaGetLastError();
 }
 

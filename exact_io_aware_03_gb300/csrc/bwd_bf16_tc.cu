@@ -572,13 +572,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       ok = wait_warp(bars.dq_full, 0, wc, ERR_WAIT_EPILOGUE);
       tc_fence_after();
     }
-    // ---- dK, dV of this key tile (this warpgroup's half of the columns)
-    if (ok && it == n) {
+    // ---- dK, dV of this key tile. Each thread reads its key row (this
+    // warpgroup's half of the columns) out of TMEM and stages it in shared
+    // memory (the Q stages, free once every MMA is done) as the 128-byte-
+    // swizzled 64-column boxes TMA uses; one thread then stores the tiles
+    // with TMA, and the CTA waits only until TMA has read them, so the
+    // global writes drain while the next CTA starts. A packed sequence's
+    // ragged last tile is written with plain coalesced stores instead (a
+    // 128-row box would run into the next sequence's rows).
+    const bool do_epi = ok && it == n;
+    uint8_t* stage = smem + C::OFF_Q;   // [dV, dK][D/64 boxes][128 keys][128 B]
+    if (do_epi) {
       const bool have = n > 0;
-      const size_t base = ((size_t)sv.hk * sv.krows + sv.k_off + key) * D + h * HD;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {   // 0: dV, 1: dK
-        uint16_t* dst = (which ? a.dk : a.dv) + base;
         const float mul = which ? p.scale : 1.f;
 #pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -594,11 +601,44 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
             pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]) * mul, __uint_as_float(x[e + 1]) * mul);
-          if (key < Nk) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+          const int col = h * HD + c0;   // first column of these 32
+          uint8_t* rowp = stage + which * C::TILE + (col / 64) * C::SUB + r * 128;
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              d4[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const int j = (col % 64) / 8 + v4;
+            *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) * 16)) =
+                make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+          }
+        }
+      }
+      fence_proxy_async_smem();   // the generic-proxy writes, before TMA reads them
+    }
+    // every compute thread arrives here; the tiles are written only if every
+    // warp staged its part
+    if (named_bar_and(1, 2 * kT, do_epi)) {
+      const bool ragged = p.cu_k != nullptr && key0 + kT > Nk;
+      if (!ragged) {
+        if (threadIdx.x == 0) {
+#pragma unroll
+          for (int which = 0; which < 2; ++which)
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_store_3d(which ? &a.tm_dk : &a.tm_dv, stage + which * C::TILE + c * C::SUB,
+                           c * 64, sv.k_off + key0, sv.hk);
+          bulk_commit_group();
+          bulk_wait_group_read0();   // shared memory may be released
+        }
+      } else {
+        constexpr int CPR = D / 8;   // 16-byte pieces per row
+        for (int idx = threadIdx.x; idx < 2 * kT * CPR; idx += 2 * kT) {
+          const int which = idx / (kT * CPR), rem = idx % (kT * CPR);
+          const int row = rem / CPR, c = rem % CPR;
+          if (key0 + row < Nk) {
+            const uint4 v = *reinterpret_cast<const uint4*>(
+                stage + which * C::TILE + (c / 8) * C::SUB + row * 128 + (((c % 8) ^ (row & 7)) * 16));
+            uint16_t* dst = (which ? a.dk : a.dv) +
+                            ((size_t)sv.hk * sv.krows + sv.k_off + key0 + row) * D + c * 8;
+            *reinterpret_cast<uint4*>(dst) = v;
           }
         }
       }

@@ -392,16 +392,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       if (i + 1 < n && !(ok = compute_p(i + 1))) break;
     }
     // ---- dQ = scale * (dS K summed over the key tiles), bf16; rows that see
-    // no key get 0. (Warp-uniform control flow: the TMEM loads are
-    // warp-collective; only the stores depend on the row.)
-    if (ok && i == n) {
+    // no key get 0. Staged in the Q buffer (Q_i lives in TMEM, so the
+    // buffer is free) as the 128-byte-swizzled boxes TMA uses and stored by
+    // one thread with TMA; a packed sequence's ragged last tile gets plain
+    // coalesced stores. (Warp-uniform control flow: the TMEM loads and the
+    // named barrier are collective.)
+    bool do_epi = ok && i == n && q0 < Nq;
+    uint8_t* stage = smem + C::OFF_Q;   // [D/64 boxes][128 rows][128 B]
+    if (do_epi) {
       const bool have = n > 0;
       if (have) {
-        if (!wait_warp(dq_full, 0, wc, ERR_WAIT_EPILOGUE)) ok = false;
+        do_epi = wait_warp(dq_full, 0, wc, ERR_WAIT_EPILOGUE);
         tc_fence_after();
       }
-      if (ok) {
-        uint16_t* dst = a.dq + ((size_t)sv.hq * sv.qrows + sv.q_off + row) * D + h * HD;
+      if (do_epi) {
 #pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
           uint32_t x[32];
@@ -417,11 +421,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
           for (int e = 0; e < 32; e += 2)
             pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]) * p.scale,
                                      __uint_as_float(x[e + 1]) * p.scale);
-          if (row < Nq) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+          const int col = h * HD + c0;
+          uint8_t* rowp = stage + (col / 64) * C::SUB + r * 128;
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              d4[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const int j = (col % 64) / 8 + v4;
+            *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) * 16)) =
+                make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+    }
+    if (named_bar_and(1, 2 * kT, do_epi)) {
+      if (p.cu_q == nullptr || q0 + kT <= Nq) {
+        if (threadIdx.x == 0) {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_store_3d(&a.tm_dq, stage + c * C::SUB, c * 64, sv.q_off + q0, sv.hq);
+          bulk_commit_group();
+          bulk_wait_group_read0();   // shared memory may be released
+        }
+      } else {
+        constexpr int CPR = D / 8;
+        for (int idx = threadIdx.x; idx < kT * CPR; idx += 2 * kT) {
+          const int rw = idx / CPR, c = idx % CPR;
+          if (q0 + rw < Nq) {
+            const uint4 v = *reinterpret_cast<const uint4*>(
+                stage + (c / 8) * C::SUB + rw * 128 + (((c % 8) ^ (rw & 7)) * 16));
+            *reinterpret_cast<uint4*>(a.dq + ((size_t)sv.hq * sv.qrows + sv.q_off + q0 + rw) * D +
+                                      c * 8) = v;
           }
         }
       }

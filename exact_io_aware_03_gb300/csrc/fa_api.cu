@@ -152,6 +152,7 @@ fa_status fwd_bf16_setup(fa::FwdBf16Args* a, const fa::Problem& p, const void* q
   if ((st = make_map(&a->tm_q, q, BH, p.Nq, p.d)) != FA_OK) return st;
   if ((st = make_map(&a->tm_k, k, p.B * p.Hkv, p.Nk, p.d)) != FA_OK) return st;
   if ((st = make_map(&a->tm_v, v, p.B * p.Hkv, p.Nk, p.d)) != FA_OK) return st;
+  if ((st = make_map(&a->tm_o, o, BH, p.Nq, p.d)) != FA_OK) return st;
   a->bias = key_bias;
   a->o = static_cast<uint16_t*>(o);
   a->lse = lse;
@@ -226,6 +227,7 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
   if ((st = make_map(&a.tm_q, q, H, total_q, d)) != FA_OK) return st;
   if ((st = make_map(&a.tm_k, k, H_kv, total_k, d)) != FA_OK) return st;
   if ((st = make_map(&a.tm_v, v, H_kv, total_k, d)) != FA_OK) return st;
+  if ((st = make_map(&a.tm_o, o, H, total_q, d)) != FA_OK) return st;
   a.o = static_cast<uint16_t*>(o);
   a.lse = lse;
   a.n_split = 1;
@@ -340,6 +342,9 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
     if ((st = make_map(&a.tm_k, k, kh, kn, d)) != FA_OK) return st;
     if ((st = make_map(&a.tm_v, v, kh, kn, d)) != FA_OK) return st;
     if ((st = make_map(&a.tm_do, dO, qh, qn, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_dk, dk, kh, kn, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_dv, dv, kh, kn, d)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_dq, dq, qh, qn, d)) != FA_OK) return st;
   }
   a.o = static_cast<const uint16_t*>(o);
   a.dO = static_cast<const uint16_t*>(dO);

@@ -70,6 +70,7 @@ struct FwdF32Args {
 struct FwdBf16Args {
   Problem p;
   CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_o;    // output, same view as tm_q (TMA stores)
   const float* bias;   // [B][Nk] or nullptr
   uint16_t* o;         // bf16 [B][H][Nq][d]
   float* lse;
@@ -84,6 +85,7 @@ struct BwdBf16Args {
   Problem p;
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
   CUtensorMap tm_dqacc;   // fp32 dQ accumulator as (d, Nq, B*H), box (32, 32, 1), 128B swizzle
+  CUtensorMap tm_dk, tm_dv, tm_dq;   // outputs, same views as tm_k / tm_q (TMA stores)
   const uint16_t* o;
   const uint16_t* dO;
   const float* lse;

@@ -490,32 +490,70 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         }
       }
       if (row_g < Nq) a.part_lse[prow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-    } else if (completed) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const size_t orow_idx = (size_t)sv.hq * sv.qrows + sv.q_off + row_g;
-      uint16_t* orow = a.o + orow_idx * D;
+    }
+    if (a.n_split <= 1) {
+      // O = O_acc / l in bf16, staged in this tile's Q buffer (free: every
+      // S product of the tile is done) as the 128-byte-swizzled 64-column
+      // boxes TMA uses, then stored with TMA by one thread of the
+      // warpgroup; the CTA waits only until TMA has read the buffer. A
+      // packed sequence's ragged last tile gets plain coalesced stores (a
+      // 128-row box would run into the next sequence).
+      const int r0 = q_base + t * kBM;
+      const bool do_epi = completed && r0 < Nq;
+      uint8_t* stage = smem + C::OFF_Q + t * C::TILE;
+      if (do_epi) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t ov[32];
-        if (have_o) {
-          tmem_ld32(lane_base + o_col + c0, ov);
-          tmem_ld_wait();
-        } else {
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ov[32];
+          if (have_o) {
+            tmem_ld32(lane_base + o_col + c0, ov);
+            tmem_ld_wait();
+          } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) ov[c] = 0u;
+            for (int c = 0; c < 32; ++c) ov[c] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2)
+            pk[c / 2] = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+          uint8_t* rowp = stage + (c0 / 64) * C::SUB + r * 128;
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const int j = (c0 % 64) / 8 + v4;
+            *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) * 16)) =
+                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
         }
-        uint32_t pk[16];
+        if (row_g < Nq)
+          a.lse[(size_t)sv.hq * sv.qrows + sv.q_off + row_g] =
+              l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        fence_proxy_async_smem();   // generic-proxy writes, before TMA reads them
+      }
+      // all 128 threads of the warpgroup arrive; the tile is written only if
+      // every warp staged its rows
+      if (named_bar_and(1 + t, kBM, do_epi)) {
+        if (p.cu_q == nullptr || r0 + kBM <= Nq) {
+          if (r == 0) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          pk[c / 2] = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
-        if (row_g < Nq) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            for (int c = 0; c < D / 64; ++c)
+              tma_store_3d(&a.tm_o, stage + c * C::SUB, c * 64, sv.q_off + r0, sv.hq);
+            bulk_commit_group();
+            bulk_wait_group_read0();   // shared memory may be released
+          }
+        } else {
+          constexpr int CPR = D / 8;   // 16-byte pieces per row
+          for (int idx = r; idx < kBM * CPR; idx += kBM) {
+            const int row = idx / CPR, c = idx % CPR;
+            if (r0 + row < Nq) {
+              const uint4 v = *reinterpret_cast<const uint4*>(
+                  stage + (c / 8) * C::SUB + row * 128 + (((c % 8) ^ (row & 7)) * 16));
+              *reinterpret_cast<uint4*>(a.o + ((size_t)sv.hq * sv.qrows + sv.q_off + r0 + row) * D +
+                                        c * 8) = v;
+            }
+          }
         }
       }
-      if (row_g < Nq) a.lse[orow_idx] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 

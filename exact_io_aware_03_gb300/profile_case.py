@@ -2,9 +2,10 @@
 
     python -m exact_io_aware_03_gb300.profile_case --workload NAME [--pass fwd|bwd|both]
                                                    [--iters N] [--causal 0|1]
+                                                   [--deterministic]
 
 Inputs are the seeded synthetic tensors of `workloads.py`. Each iteration runs
-fa_fwd and/or fa_bwd once on the current stream; the script synchronises and
+fa_fwd and/or fa_bwd (or fa_bwd_deterministic) once on the current stream; the script synchronises and
 checks the device error word at the end. Nothing is timed or compared: this
 is the small, self-contained command to put under `ncu`.
 """
@@ -31,6 +32,8 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=2)
     ap.add_argument("--causal", type=int, choices=[0, 1], default=None,
                     help="override the workload's causal flag")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="run fa_bwd_deterministic instead of fa_bwd")
     args = ap.parse_args(argv)
 
     w = workloads.WORKLOADS[args.workload]
@@ -45,14 +48,16 @@ def main(argv=None):
     kw = dict(key_bias=bias, causal=w.causal, scale=w.scale)
     o, lse = fa.fwd(q, k, v, **kw)
     if w.dtype == "bf16":
-        ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d), dtype=torch.uint8,
-                         device=dev)
+        ws_bytes = (fa.fa_bwd_deterministic_workspace_size(w.B, w.H, w.Nq, w.d)
+                    if args.deterministic else fa.fa_bwd_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d))
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     for _ in range(args.iters):
         if args.which in ("fwd", "both"):
             fa.fwd(q, k, v, out=o, lse=lse, **kw)
         if args.which in ("bwd", "both") and w.dtype == "bf16":
-            fa.bwd(q, k, v, o, lse, dO, workspace=ws, dq=dq, dk=dk, dv=dv, **kw)
+            fa.bwd(q, k, v, o, lse, dO, workspace=ws, dq=dq, dk=dk, dv=dv,
+                   deterministic=args.deterministic, **kw)
     torch.cuda.synchronize(dev)
     fa.check_device_error(dev)
     print("ok: %s %s x%d" % (w.name, args.which, args.iters))

@@ -408,49 +408,54 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     uint8_t* ds_s = smem + C::OFF_DS;
     constexpr int HD = D / 2;      // dQ / dK / dV columns per warpgroup
 
-    // dQ of query tile `it` (TMEM lane = query row): read this warpgroup's
-    // columns, hand the TMEM region back, scale, and reduce-add them into the
-    // fp32 accumulator with TMA: each warp stages its 32 rows as 128-byte-
-    // swizzled boxes of 32 columns (4 KiB each) in its own slice of the dS
-    // buffer (free here: the dQ product that read it has completed) and of a
-    // second staging area; it rewrites them only after TMA has read them.
-    // chunk 0 in this warp's slice of the dS boxes, chunk 1 in its slice of
-    // the second staging area
-    uint8_t* stage0 = ds_s + warp * 4096;
-    uint8_t* stage1 = smem + C::OFF_DQST + warp * 4096;
-    auto dq_readout = [&](int it) -> bool {
-      if (!wait_warp(bars.dq_full, it & 1, wc, ERR_WAIT_EPILOGUE)) return false;
-      tc_fence_after();
-      uint32_t x[HD];
+    // dQ of query tile `it` (TMEM lane = query row): this warpgroup's columns
+    // are read out of TMEM at once (the columns go back to the MMA warp),
+    // scaled, and reduce-added into the fp32 accumulator with TMA in boxes
+    // of 32 rows x 32 columns (4 KiB, 128-byte swizzled) staged in this
+    // warp's slot of the staging buffer. A TMA reduction reads its box at
+    // ~25 B/clock, so a warp stages its first box right away and keeps the
+    // second in registers until after the next tile's dS (by then the first
+    // box has been read): nothing waits on the reductions, and the dS
+    // buffer is never used for staging.
+    uint8_t* dq_stage = smem + C::OFF_DQST + warp * 4096;
+    uint32_t dq_hold[32];   // second box of the pending dQ (d = 128)
+    int hold_row0 = 0, hold_qc = 0;
+    auto stage_box = [&](const uint32_t* v32, int col, int row0, int qc) {
+      if (lane == 0) bulk_wait_group_read0();   // the previous box has been read
+      __syncwarp();
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) tmem_ld32(lane_base + 128 + h * HD + c * 32, x + c * 32);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(bars.dq_empty);
-      const int row0 = sv.q_off + q_row0(it) + (warp % 4) * 32;
-      const int qc = q_coord(q_head(it));
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        uint8_t* stage = c == 0 ? stage0 : stage1;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t* v = x + c * 32 + 4 * k;
-          *reinterpret_cast<uint4*>(stage + lane * 128 + ((k ^ (lane & 7)) * 16)) = make_uint4(
-              __float_as_uint(__uint_as_float(v[0]) * p.scale),
-              __float_as_uint(__uint_as_float(v[1]) * p.scale),
-              __float_as_uint(__uint_as_float(v[2]) * p.scale),
-              __float_as_uint(__uint_as_float(v[3]) * p.scale));
-        }
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t* v = v32 + 4 * k;
+        *reinterpret_cast<uint4*>(dq_stage + lane * 128 + ((k ^ (lane & 7)) * 16)) = make_uint4(
+            __float_as_uint(__uint_as_float(v[0]) * p.scale),
+            __float_as_uint(__uint_as_float(v[1]) * p.scale),
+            __float_as_uint(__uint_as_float(v[2]) * p.scale),
+            __float_as_uint(__uint_as_float(v[3]) * p.scale));
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-#pragma unroll
-        for (int c = 0; c < HD / 32; ++c)
-          tma_reduce_add_3d(&a.tm_dqacc, c == 0 ? stage0 : stage1, h * HD + c * 32, row0, qc);
+        tma_reduce_add_3d(&a.tm_dqacc, dq_stage, col, row0, qc);
+        bulk_commit_group();
       }
-      if (lane == 0) bulk_commit_group();
+    };
+    auto dq_readout = [&](int it) -> bool {
+      if (!wait_warp(bars.dq_full, it & 1, wc, ERR_WAIT_EPILOGUE)) return false;
+      tc_fence_after();
+      uint32_t x[32];
+      tmem_ld32(lane_base + 128 + h * HD, x);
+      if constexpr (HD > 32) tmem_ld32(lane_base + 128 + h * HD + 32, dq_hold);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(bars.dq_empty);
+      hold_row0 = sv.q_off + q_row0(it) + (warp % 4) * 32;
+      hold_qc = q_coord(q_head(it));
+      stage_box(x, h * HD, hold_row0, hold_qc);
       return true;
+    };
+    // the second box of the pending dQ (no-op at d = 64, which has one)
+    auto dq_finish = [&]() {
+      if constexpr (HD > 32) stage_box(dq_hold, h * HD + 32, hold_row0, hold_qc);
     };
     // P^T of query tile `it` = exp2(S^T * scale*log2e + bias - LSE2), masked
     // -> 0, kept in fp32 registers for dS; packed bf16 copy to TMEM for dV.
@@ -529,11 +534,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           // already read (chunk 0 -> columns [0,16), chunk 1 -> [16,32))
           tmem_st16(lane_base + 128 + h * 64 + half * 16, dsk);
         } else {
-          if (half == 0) {
-            // the staged dQ of the previous tile must have been read by TMA
-            if (lane == 0) bulk_wait_group_read0();
-            __syncwarp();
-          }
           // row = key of the 128-byte-swizzled box holding query columns
           // [64h, 64h+64); this chunk is its 16-byte pieces 4*half .. 4*half+3
           uint8_t* rowp = ds_s + h * C::SUB + r * 128;
@@ -555,16 +555,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       return true;
     };
 
-    // Order per tile i: dS(i), then P(i+1) (its S^T was issued right after
-    // dV(i)), then the read-out of dQ(i); P(0) first.
+    // Order per tile i: dS(i), the second dQ box of tile i-1, P(i+1) (its
+    // S^T was issued right after dV(i)), then the read-out of dQ(i); P(0)
+    // first.
     int it = 0;
     bool ok = n == 0 || compute_p(0);
     for (; ok && it < n; ++it) {
       if (!(ok = compute_ds(it))) break;
+      if (!DET && it > 0) dq_finish();
       if (it + 1 < n && !(ok = compute_p(it + 1))) break;
       if (!DET && !(ok = dq_readout(it))) break;   // the last one: every MMA of this CTA is done
     }
     if (!DET) {
+      if (ok && it == n && n > 0) dq_finish();
       if (lane == 0) bulk_wait_group0();   // reductions complete before the CTA exits
       __syncwarp();
     } else if (ok && it == n && n > 0) {

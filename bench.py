@@ -476,6 +476,39 @@ def run_ours(args):
         ms_g = b0.elapsed_time(b1) / n_e
         extras["gqa_b4h16kv4_n4096_d128_causal_fwdbwd_tflops"] = (f_fwd + f_bwd) / (ms_g * 1e-3) / 1e12
         del qg, dOg, kg, vg, og, lg, dqg, dkg, dvg
+        # FP8 forward on the long-context workload: the e4m3 quantization and
+        # the attention (e4m3 MMAs) timed apart; the attention against the
+        # fp8 peak (2x the measured bf16 peak: the nominal fp8/bf16 ratio)
+        qe, ke, ve = (torch.randn((we.B, we.H, we.Nq, we.d), generator=g, device=dev,
+                                  dtype=torch.bfloat16) for _ in range(3))
+        oe = torch.empty_like(qe)
+        le = torch.empty(qe.shape[:3], dtype=torch.float32, device=dev)
+        ws8 = torch.empty(fa.fa_fwd_fp8_workspace_size(we.B, we.H, we.H, we.Nq, we.Nk, we.d),
+                          dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            fa.fwd_fp8(qe, ke, ve, causal=True, out=oe, lse=le, workspace=ws8)
+        ev8 = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        t_q, t_a = [], []
+        for _ in range(n_e):
+            ev8[0].record(stream)
+            fa.fwd_fp8(qe, ke, ve, causal=True, out=oe, lse=le, workspace=ws8, stage=1)
+            ev8[1].record(stream)
+            fa.fwd_fp8(qe, ke, ve, causal=True, out=oe, lse=le, workspace=ws8, stage=2)
+            ev8[2].record(stream)
+            torch.cuda.synchronize(dev)
+            t_q.append(ev8[0].elapsed_time(ev8[1]))
+            t_a.append(ev8[1].elapsed_time(ev8[2]))
+        fa.check_device_error(dev)
+        f_e = flops(we)[0]
+        fp8_peak = 2.0 * load_peaks()[0].get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        ms_a, ms_q = statistics.median(t_a), statistics.median(t_q)
+        extras["fp8_" + we.name + "_fwd"] = {
+            "attention_ms": ms_a, "quantize_ms": ms_q,
+            "attention_tflops": f_e / (ms_a * 1e-3) / 1e12,
+            "frac_of_fp8_peak": f_e / (ms_a * 1e-3) / 1e12 / fp8_peak,
+            "with_quantize_tflops": f_e / ((ms_a + ms_q) * 1e-3) / 1e12,
+            "fp8_peak_tflops": fp8_peak}
+        del qe, ke, ve, oe, le, ws8
         # deterministic backward (query-outer dQ kernel, no reductions) on the
         # benchmark workload, timed per launch
         wsd = torch.empty(fa.fa_bwd_deterministic_workspace_size(w.B, w.H, w.Nq, w.d),

@@ -65,6 +65,13 @@ def load(path=None):
                                cint, cint, cf, cint, cint, vp, csz, vp]
     lib.fa_bwd_gqa.restype = cint
     lib.fa_fwd_splitkv.restype = cint
+    lib.fa_fwd_fp8_workspace_size.argtypes = [cint] * 6
+    lib.fa_fwd_fp8_workspace_size.restype = csz
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, cint, cint, cint, cint, cint, cint, cf,
+                               cint, vp, csz, vp]
+    lib.fa_fwd_fp8.restype = cint
+    lib.fa_fwd_fp8_stage.argtypes = list(lib.fa_fwd_fp8.argtypes) + [cint]
+    lib.fa_fwd_fp8_stage.restype = cint
     lib.fa_bwd_deterministic_workspace_size.argtypes = [cint] * 4
     lib.fa_bwd_deterministic_workspace_size.restype = csz
     lib.fa_bwd_deterministic.argtypes = list(lib.fa_bwd_gqa.argtypes)
@@ -128,6 +135,22 @@ def fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d,
                dtype, workspace, workspace_bytes, stream):
     return load().fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, key_bias, B, H, H_kv, Nq, Nk, d,
                              scale, causal, dtype, workspace, workspace_bytes, stream)
+
+
+def fa_fwd_fp8_workspace_size(B, H, H_kv, Nq, Nk, d):
+    return load().fa_fwd_fp8_workspace_size(B, H, H_kv, Nq, Nk, d)
+
+
+def fa_fwd_fp8(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal, workspace,
+               workspace_bytes, stream):
+    return load().fa_fwd_fp8(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal,
+                             workspace, workspace_bytes, stream)
+
+
+def fa_fwd_fp8_stage(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal, workspace,
+                     workspace_bytes, stream, stage):
+    return load().fa_fwd_fp8_stage(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal,
+                                   workspace, workspace_bytes, stream, stage)
 
 
 def fa_bwd_deterministic_workspace_size(B, H, Nq, d):
@@ -272,6 +295,32 @@ def fwd(q, k, v, key_bias=None, causal=False, scale=None, out=None, lse=None):
                         _stream(q))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_gqa")
+    return out, lse
+
+
+def fwd_fp8(q, k, v, key_bias=None, causal=False, scale=None, out=None, lse=None, workspace=None,
+            stage=0):
+    """FP8 forward (fa_fwd_fp8): bf16 q, k, v quantized to e4m3 per head into
+    ``workspace``, attention on the tensor cores' fp8 path; bf16 O, fp32 LSE.
+    stage: 0 both, 1 quantization only, 2 attention only (from the workspace)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if workspace is None:
+        workspace = torch.empty(fa_fwd_fp8_workspace_size(B, H, Hkv, Nq, Nk, d), dtype=torch.uint8,
+                                device=q.device)
+    with torch.cuda.device(q.device):
+        st = fa_fwd_fp8_stage(_ptr(q), _ptr(k), _ptr(v), _ptr(key_bias), _ptr(out), _ptr(lse), B, H,
+                              Hkv, Nq, Nk, d, float(scale), int(bool(causal)), _ptr(workspace),
+                              workspace.numel(), _stream(q), int(stage))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_fp8")
     return out, lse
 
 

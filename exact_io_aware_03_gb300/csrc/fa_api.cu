@@ -109,6 +109,39 @@ fa_status make_map_f32_acc(CUtensorMap* m, const void* base, int BH, int N, int 
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// 3-D view (dim0, dim1, dim2) of a byte tensor with rows of dim0 bytes, box
+// (128, 128, 1), 128-byte swizzle, zero fill outside (the e4m3 operands).
+fa_status make_map_u8(CUtensorMap* m, const void* base, long dim0, long dim1, long dim2) {
+  EncodeTiledFn enc = nullptr;
+  fa_status st = get_encode(&enc);
+  if (st != FA_OK) return st;
+  cuuint64_t dims[3] = {(cuuint64_t)dim0, (cuuint64_t)dim1, (cuuint64_t)dim2};
+  cuuint64_t strides[2] = {(cuuint64_t)dim0, (cuuint64_t)(dim0 * dim1)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// Workspace of the e4m3 forward: per-head max |x| (q, k, v), e4m3 q, k, and
+// the transposed e4m3 v with keys padded to a multiple of 16; each part on a
+// 256-byte boundary.
+struct Fp8Ws {
+  size_t amax, q8, k8, vt8, total;
+};
+Fp8Ws fp8_ws_layout(int B, int H, int Hkv, int Nq, int Nk, int d) {
+  Fp8Ws w;
+  const size_t nk16 = ((size_t)Nk + 15) / 16 * 16;
+  w.amax = 0;
+  w.q8 = round256(4 * ((size_t)B * H + 2 * (size_t)B * Hkv));
+  w.k8 = w.q8 + round256((size_t)B * H * Nq * d);
+  w.vt8 = w.k8 + round256((size_t)B * Hkv * Nk * d);
+  w.total = w.vt8 + round256((size_t)B * Hkv * d * nk16);
+  return w;
+}
+
 // Workspace of the backward: padded statistics for B*H (sequence, head)
 // pairs of nq_max rows, then the fp32 dQ accumulator of `dq_rows` rows.
 size_t bwd_ws_bytes(int B, int H, int nq_max, size_t dq_rows, int d) {
@@ -470,6 +503,77 @@ fa_status fa_bwd_varlen_deterministic(const void* q, const void* k, const void* 
                     max_seqlen_k, d, scale, causal, FA_DTYPE_BF16, workspace, workspace_bytes,
                     stream, fa::BWD_PRE | fa::BWD_MAIN | fa::BWD_DQ | fa::BWD_DET, cu_seqlens_q,
                     cu_seqlens_k, total_q, total_k);
+}
+
+size_t fa_fwd_fp8_workspace_size(int B, int H, int H_kv, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || H_kv < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
+  return fp8_ws_layout(B, H, H_kv, Nq, Nk, d).total;
+}
+
+fa_status fa_fwd_fp8_stage(const void* q, const void* k, const void* v, const float* key_bias,
+                           void* o, float* lse, int B, int H, int H_kv, int Nq, int Nk, int d,
+                           float scale, int causal, void* workspace, size_t workspace_bytes,
+                           void* stream, int stage) {
+  if (stage < 0 || stage > 2) return FA_ERR_INVALID_ARG;
+  fa_status st = check_problem(B, H, Nq, Nk, d, scale, FA_DTYPE_BF16, H_kv);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || (key_bias && !aligned(key_bias, 4)) || !aligned(workspace, 256))
+    return FA_ERR_INVALID_ARG;
+  const Fp8Ws w = fp8_ws_layout(B, H, H_kv, Nq, Nk, d);
+  if (workspace_bytes < w.total) return FA_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace);
+  float* amax = reinterpret_cast<float*>(ws + w.amax);
+  const int nk16 = (Nk + 15) / 16 * 16;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (stage == 0 || stage == 1) {
+    fa::QuantFp8Args qa;
+    qa.q = static_cast<const uint16_t*>(q);
+    qa.k = static_cast<const uint16_t*>(k);
+    qa.v = static_cast<const uint16_t*>(v);
+    qa.q8 = reinterpret_cast<uint8_t*>(ws + w.q8);
+    qa.k8 = reinterpret_cast<uint8_t*>(ws + w.k8);
+    qa.vt8 = reinterpret_cast<uint8_t*>(ws + w.vt8);
+    qa.amax_q = amax;
+    qa.amax_k = amax + (size_t)B * H;
+    qa.amax_v = amax + (size_t)B * H + (size_t)B * H_kv;
+    qa.heads_q = B * H;
+    qa.heads_kv = B * H_kv;
+    qa.Nq = Nq;
+    qa.Nk = Nk;
+    qa.nk16 = nk16;
+    qa.d = d;
+    if (cudaMemsetAsync(amax, 0, w.q8, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_quant_fp8(qa, s) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  if (stage == 0 || stage == 2) {
+    fa::FwdBf16Args a;
+    std::memset(&a, 0, sizeof(a));
+    a.p = fa::Problem{B, H, Nq, Nk, d, scale, causal ? 1 : 0, H_kv};
+    if ((st = make_map_u8(&a.tm_q, ws + w.q8, d, Nq, (long)B * H)) != FA_OK) return st;
+    if ((st = make_map_u8(&a.tm_k, ws + w.k8, d, Nk, (long)B * H_kv)) != FA_OK) return st;
+    if ((st = make_map_u8(&a.tm_v, ws + w.vt8, nk16, d, (long)B * H_kv)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_o, o, B * H, Nq, d)) != FA_OK) return st;
+    a.bias = key_bias;
+    a.o = static_cast<uint16_t*>(o);
+    a.lse = lse;
+    a.n_split = 1;
+    a.amax_q = amax;
+    a.amax_k = amax + (size_t)B * H;
+    a.amax_v = amax + (size_t)B * H + (size_t)B * H_kv;
+    if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
+    if (fa::launch_fwd_fp8(a, s) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, const float* key_bias, void* o,
+                     float* lse, int B, int H, int H_kv, int Nq, int Nk, int d, float scale,
+                     int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa_fwd_fp8_stage(q, k, v, key_bias, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal,
+                          workspace, workspace_bytes, stream, 0);
 }
 
 fa_status fa_selftest_device_timeout(void* stream) {

@@ -79,7 +79,16 @@ struct FwdBf16Args {
   int n_split;         // split-KV: number of key ranges (1 = off)
   float* part_o;       // split-KV workspace: fp32 O [n_split][B*H][Nq][d]
   float* part_lse;     // split-KV workspace: LSE [n_split][B*H][Nq]
+  // e4m3 forward: per-head max |x| of q [B*H], k and v [B*Hkv] (tm_q, tm_k
+  // then view the e4m3 q, k and tm_v the transposed e4m3 v [B*Hkv][d][Nk16])
+  const float* amax_q;
+  const float* amax_k;
+  const float* amax_v;
 };
+
+// Per-head e4m3 scale: x ~= scale * e4m3(x / scale), scale = max|x| / 448
+// (448 = the largest finite e4m3 value), 1 for an all-zero head.
+__host__ __device__ inline float fp8_scale(float amax) { return amax > 0.f ? amax / 448.f : 1.f; }
 
 struct BwdBf16Args {
   Problem p;
@@ -105,6 +114,24 @@ struct BwdBf16Args {
 
 cudaError_t launch_fwd_f32(const FwdF32Args& a, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const FwdBf16Args& a, cudaStream_t s);
+// e4m3 forward (d = 128, dense, no split): amax_* and the e4m3 tensor maps set.
+cudaError_t launch_fwd_fp8(const FwdBf16Args& a, cudaStream_t s);
+// Per-head max |x| of q [B*H rows_q d], k, v [B*Hkv rows_k d] into amax (zeroed
+// by the caller), then q, k -> e4m3 (same layout) and v -> e4m3 transposed
+// [B*Hkv][d][nk16] (keys past Nk zero).
+struct QuantFp8Args {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  uint8_t* q8;
+  uint8_t* k8;
+  uint8_t* vt8;
+  float* amax_q;   // [B*H]
+  float* amax_k;   // [B*Hkv]
+  float* amax_v;   // [B*Hkv]
+  int heads_q, heads_kv, Nq, Nk, nk16, d;
+};
+cudaError_t launch_quant_fp8(const QuantFp8Args& a, cudaStream_t s);
 // Backward stages (bit mask): D / base-2 LSE / zeroed dQ accumulator; the
 // tensor-core main loop; the dQ conversion. BWD_DET selects the deterministic
 // variant of the main loop (dK, dV only; no accumulator is zeroed when dq_acc

@@ -57,15 +57,22 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int D>
+// FP8: q, k are e4m3 [rows][d] and v is e4m3 transposed, [d][keys] (every
+// operand K-major), with per-head scales; d = 128 only (one 128-byte row).
+template <int D, bool FP8>
 struct FwdCfg {
-  static constexpr int NS = (D == 128) ? 2 : 4;            // K/V ring stages
-  static constexpr int TILE = kBM * D * 2;                 // bytes of one bf16 tile
-  static constexpr int SUB = kBM * 128;                    // bytes of one 64-column box
+  static constexpr int EB = FP8 ? 1 : 2;                   // element bytes of q, k, v
+  static constexpr int NS = FP8 ? 3 : ((D == 128) ? 2 : 4);   // K/V ring stages
+  static constexpr int TILE = kBM * D * EB;                // bytes of one q/k/v tile
+  static constexpr int SUB = kBM * 128;                    // bytes of one 128-byte-wide box
+  static constexpr int NBOX = D * EB / 128;                // boxes per tile
+  static constexpr int OTILE = kBM * D * 2;                // bf16 O tile (epilogue staging)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_MISC = OFF_V + NS * TILE;
+  // O staging: the Q buffers (bf16), or a buffer of its own (FP8 tiles are smaller)
+  static constexpr int OFF_OST = FP8 ? OFF_V + NS * TILE : OFF_Q;
+  static constexpr int OFF_MISC = FP8 ? OFF_OST + 2 * OTILE : OFF_V + NS * TILE;
   // misc: bias buffers [2 tiles][2 bufs][128] floats, then barriers
   static constexpr int OFF_BIAS = OFF_MISC;
   static constexpr int OFF_BAR = OFF_BIAS + 2 * 2 * kBN * 4;
@@ -89,9 +96,9 @@ struct Bars {
   uint64_t* drain;     // [1]
 };
 
-template <int D>
+template <int D, bool FP8>
 __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, FP8>;
   uint64_t* b = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   Bars r;
   r.q_full = b; b += 2;
@@ -107,9 +114,9 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   return r;
 }
 
-template <int D, bool CAUSAL, bool BIAS>
-__global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdBf16Args a) {
-  using C = FwdCfg<D>;
+template <int D, bool CAUSAL, bool BIAS, bool FP8>
+__device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
+  using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -117,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
 
-  Bars bars = carve_bars<D>(smem);
+  Bars bars = carve_bars<D, FP8>(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_SCALARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SCALARS + 4);
   int* key_lo_s = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 8);
@@ -242,27 +249,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       for (int t = 0; t < 2; ++t) {
         if (hi_t[t] <= lo) continue;
         mbar_arrive_expect_tx(&bars.q_full[t], C::TILE);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(q_s + t * C::TILE + c * C::SUB, &a.tm_q, c * 64, sv.q_off + q_base + t * kBM,
-                      sv.hq,
-                      &bars.q_full[t]);
+        for (int c = 0; c < C::NBOX; ++c)
+          tma_load_3d(q_s + t * C::TILE + c * C::SUB, &a.tm_q, c * (128 / C::EB),
+                      sv.q_off + q_base + t * kBM, sv.hq, &bars.q_full[t]);
       }
       int nk = 0, nv = 0;   // K / V fills issued
       for (int j = lo; j < hi; ++j) {
         const int i = j - lo, s = i % C::NS, u = i / C::NS;
         if (u > 0 && !wait1(&bars.k_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
         mbar_arrive_expect_tx(&bars.k_full[s], C::TILE);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::SUB, &a.tm_k, c * 64,
-                      sv.k_off + j * kBN, sv.hk,
-                      &bars.k_full[s]);
+        for (int c = 0; c < C::NBOX; ++c)
+          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::SUB, &a.tm_k, c * (128 / C::EB),
+                      sv.k_off + j * kBN, sv.hk, &bars.k_full[s]);
         ++nk;
         if (u > 0 && !wait1(&bars.v_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
         mbar_arrive_expect_tx(&bars.v_full[s], C::TILE);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::SUB, &a.tm_v, c * 64,
-                      sv.k_off + j * kBN, sv.hk,
-                      &bars.v_full[s]);
+        if constexpr (FP8) {
+          // V^T tile: 128 keys (bytes) x D rows
+          tma_load_3d(smem + C::OFF_V + s * C::TILE, &a.tm_v, j * kBN, 0, sv.hk, &bars.v_full[s]);
+        } else {
+          for (int c = 0; c < C::NBOX; ++c)
+            tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::SUB, &a.tm_v, c * 64,
+                        sv.k_off + j * kBN, sv.hk, &bars.v_full[s]);
+        }
         ++nv;
       }
       // Drain: wait (bounded, ignoring the abort flag) for the last fill of
@@ -280,27 +289,42 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   } else if (warp == 9) {
     // ================================================================ MMA issuer
     if (lane == 0 && any) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
+      constexpr uint32_t idesc_s =
+          FP8 ? idesc_e4m3_f32(kBM, kBN, false, false) : idesc_bf16_f32(kBM, kBN, false, false);
+      // PV: B = V (MN-major, d contiguous) or, FP8, V^T (K-major, keys contiguous)
+      constexpr uint32_t idesc_pv =
+          FP8 ? idesc_e4m3_f32(kBM, D, false, false) : idesc_bf16_f32(kBM, D, false, true);
       const uint32_t q_addr = smem_u32(smem + C::OFF_Q);
       const uint32_t k_addr = smem_u32(smem + C::OFF_K);
       const uint32_t v_addr = smem_u32(smem + C::OFF_V);
       auto active = [&](int t, int j) { return j >= lo && j < hi_t[t]; };
       auto issue_s = [&](int t, int s) {
         const uint32_t qa = q_addr + t * C::TILE, ka = k_addr + s * C::TILE;
+        // K steps of 32 bytes (16 bf16 or 32 e4m3) along the 128-byte rows
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D * C::EB / 32; ++kk) {
           const uint32_t off = (kk / 4) * C::SUB + (kk % 4) * 32;
-          mma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 idesc_s, kk > 0);
+          if constexpr (FP8)
+            mma_ss_f8(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024),
+                      sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+          else
+            mma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024),
+                   sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int s, bool acc) {
         const uint32_t va = v_addr + s * C::TILE;
+        if constexpr (FP8) {
+          // P as packed e4m3 (4 keys per TMEM column): 32 keys per K step
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
-                 sdesc_sw128(va + kk * 2048, C::SUB, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBN / 32; ++kk)
+            mma_ts_f8(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
+                      sdesc_sw128(va + kk * 32, 16, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
+                   sdesc_sw128(va + kk * 2048, C::SUB, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = true;
@@ -353,7 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     const int row_g = q_base + t * kBM + r;
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const uint32_t s_col = t * 128, o_col = 256 + t * D;
-    const float sl2 = p.scale * kLog2e;
+    // FP8: S = sq * sk * (q8 k8^T), folded into the exponent's scale
+    const float sqk = FP8 ? fp8_scale(a.amax_q[bh]) * fp8_scale(a.amax_k[sv.hk]) : 1.f;
+    const float sl2 = p.scale * sqk * kLog2e;
     const long off = (long)Nk - Nq;
     // last visible key of this row / of the tile's first row (tile-uniform)
     const long lim_row = CAUSAL ? min((long)row_g + off, (long)Nk - 1) : (long)Nk - 1;
@@ -421,18 +447,37 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       const uint64_t mul2 = scaled ? f2_pack(1.f, 1.f) : f2_pack(sl2, sl2);
       const uint64_t nmu2 = f2_pack(-mu, -mu);
       uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};   // row sum as 4 packed partial sums
+      if constexpr (FP8) {
+        // P as e4m3, 4 keys per TMEM column (p <= 2^8 fits the e4m3 range)
 #pragma unroll
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
-        uint32_t pk[16];
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          uint32_t pk[8];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float x0, x1;
-          f2_unpack(fma2(f2_pack(s[c0 + c], s[c0 + c + 1]), mul2, nmu2), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          ps2[(c / 2) & 3] = add2(ps2[(c / 2) & 3], f2_pack(p0, p1));
-          pk[c / 2] = pack_bf16x2(p0, p1);
+          for (int c = 0; c < 32; c += 4) {
+            float x0, x1, x2, x3;
+            f2_unpack(fma2(f2_pack(s[c0 + c], s[c0 + c + 1]), mul2, nmu2), x0, x1);
+            f2_unpack(fma2(f2_pack(s[c0 + c + 2], s[c0 + c + 3]), mul2, nmu2), x2, x3);
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+            ps2[(c / 2) & 3] = add2(ps2[(c / 2) & 3], f2_pack(p0, p1));
+            ps2[(c / 2 + 1) & 3] = add2(ps2[(c / 2 + 1) & 3], f2_pack(p2, p3));
+            pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
+          }
+          tmem_st8(lane_base + s_col + c0 / 4, pk);
         }
-        tmem_st16(lane_base + s_col + c0 / 2, pk);
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float x0, x1;
+            f2_unpack(fma2(f2_pack(s[c0 + c], s[c0 + c + 1]), mul2, nmu2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            ps2[(c / 2) & 3] = add2(ps2[(c / 2) & 3], f2_pack(p0, p1));
+            pk[c / 2] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(lane_base + s_col + c0 / 2, pk);
+        }
       }
       float ps[8];
 #pragma unroll
@@ -500,9 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       // 128-row box would run into the next sequence).
       const int r0 = q_base + t * kBM;
       const bool do_epi = completed && r0 < Nq;
-      uint8_t* stage = smem + C::OFF_Q + t * C::TILE;
+      uint8_t* stage = smem + C::OFF_OST + t * C::OTILE;
       if (do_epi) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        // FP8: O = sv * (P8 v8) / l
+        const float sv_ = FP8 ? fp8_scale(a.amax_v[sv.hk]) : 1.f;
+        const float inv = l > 0.f ? sv_ / l : 0.f;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t ov[32];
@@ -567,6 +614,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   }
 }
 
+template <int D, bool CAUSAL, bool BIAS>
+__global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdBf16Args a) {
+  fwd_body<D, CAUSAL, BIAS, false>(a);
+}
+
+// The same forward on e4m3 operands (kind::f8f6f4 MMAs at twice the bf16
+// rate): S from e4m3 Q, K with per-head scales, P rounded to e4m3 for PV.
+template <int D, bool CAUSAL, bool BIAS>
+__global__ void __launch_bounds__(kThreads, 1) fwd_fp8_kernel(const __grid_constant__ FwdBf16Args a) {
+  fwd_body<D, CAUSAL, BIAS, true>(a);
+}
+
 // Split-KV combine (the merge of partial softmax states over disjoint key
 // ranges: "flash-attention", Part VI; "FlashAttention: Mathematical
 // Foundations...", Flash-Decoding): with partial (O_s, LSE_s),
@@ -610,7 +669,7 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
 
 template <int D, bool CAUSAL, bool BIAS>
 cudaError_t launch_one(const FwdBf16Args& a, cudaStream_t s) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, false>;
   auto kern = fwd_bf16_kernel<D, CAUSAL, BIAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_ALLOC);
@@ -643,6 +702,32 @@ cudaError_t launch_d(const FwdBf16Args& a, cudaStream_t s) {
 
 cudaError_t launch_fwd_bf16(const FwdBf16Args& a, cudaStream_t s) {
   return a.p.d == 64 ? launch_d<64>(a, s) : launch_d<128>(a, s);
+}
+
+namespace {
+template <bool CAUSAL, bool BIAS>
+cudaError_t launch_fp8_one(const FwdBf16Args& a, cudaStream_t s) {
+  using C = FwdCfg<128, true>;
+  static_assert(C::SMEM_ALLOC <= 232448, "shared memory per CTA");
+  auto kern = fwd_fp8_kernel<128, CAUSAL, BIAS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  const long BH = (long)a.p.B * a.p.H;
+  const long n_pairs = (a.p.Nq + 2 * kBM - 1) / (2 * kBM);
+  const long kv_bytes = 2L * a.p.Nk * 128;   // e4m3 K and V of a head
+  FwdBf16Args b = a;
+  b.head_group = (int)std::max(1L, std::min(BH, (48L << 20) / std::max(kv_bytes, 1L)));
+  b.n_split = 1;
+  kern<<<(unsigned)(BH * n_pairs), kThreads, C::SMEM_ALLOC, s>>>(b);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_fwd_fp8(const FwdBf16Args& a, cudaStream_t s) {
+  const bool bias = a.bias != nullptr;
+  if (a.p.causal) return bias ? launch_fp8_one<true, true>(a, s) : launch_fp8_one<true, false>(a, s);
+  return bias ? launch_fp8_one<false, true>(a, s) : launch_fp8_one<false, false>(a, s);
 }
 
 }  // namespace fa

@@ -214,6 +214,37 @@ fa_status fa_bwd_postprocess(const void *q, const void *k, const void *v, const 
                              void *stream);
 
 /*
+ * FP8 forward ("FlashAttention, Explained", §21 and "FlashAttention:
+ * Mathematical Foundations...", the FP8 forward of FA-3: e4m3 operands with
+ * scaling factors, the matrix products at the fp8 tensor-core rate). Same
+ * arguments and results as fa_fwd_gqa (bf16 q, k, v; bf16 o, fp32 lse;
+ * d = 128 only, else FA_ERR_UNSUPPORTED), computed as:
+ *   scale_x = max|x| / 448 per (batch, head) of each of q, k, v (1 if 0),
+ *   x8 = e4m3(x / scale_x), round to nearest even;
+ *   S = scale * scale_q * scale_k * (q8 k8^T) (fp32 accumulation),
+ *   P = exp(S - m) rounded to e4m3, O = scale_v * (P v8) / rowsum(exp(S - m)),
+ *   LSE from the fp32 S.
+ * The result approximates attention on the dequantized inputs
+ * scale_x * x8; P's rounding (relative 2^-4) bounds the difference.
+ * workspace: fa_fwd_fp8_workspace_size(...) bytes, 256-byte aligned:
+ *   [0]  fp32 max|q| [B*H], max|k| [B*H_kv], max|v| [B*H_kv]
+ *   then, each on a 256-byte boundary: e4m3 q [B,H,Nq,d], e4m3 k
+ *   [B,H_kv,Nk,d], e4m3 v transposed [B,H_kv,d,Nk16] (Nk16 = Nk rounded up to
+ *   a multiple of 16, the padding 0).
+ * fa_fwd_fp8_stage runs stage 1 (quantize into the workspace) or stage 2
+ * (attention from the workspace) alone; 0 runs both (= fa_fwd_fp8).
+ */
+size_t fa_fwd_fp8_workspace_size(int B, int H, int H_kv, int Nq, int Nk, int d);
+fa_status fa_fwd_fp8(const void *q, const void *k, const void *v, const float *key_bias,
+                     void *o, float *lse,
+                     int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int causal,
+                     void *workspace, size_t workspace_bytes, void *stream);
+fa_status fa_fwd_fp8_stage(const void *q, const void *k, const void *v, const float *key_bias,
+                           void *o, float *lse,
+                           int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int causal,
+                           void *workspace, size_t workspace_bytes, void *stream, int stage);
+
+/*
  * Deterministic backward ("flash-attention", Part VII: the backward's
  * deterministic option). fa_bwd accumulates dQ over key tiles with
  * reductions whose order depends on timing, so dq may differ in the last

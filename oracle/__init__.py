@@ -312,3 +312,52 @@ def bwd_varlen(q, k, v, dO, cu_q, cu_k, scale=None, causal=False):
         dk[:, k0:k1] = gk[0]
         dv[:, k0:k1] = gv[0]
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------- e4m3
+# The FP8 forward works on e4m3 copies of q, k, v with one scale per (batch,
+# head): scale = max|x| / 448 (448 = the largest finite e4m3 value; 1 for an
+# all-zero head) and x8 = e4m3(x / scale), round to nearest even ("FlashAttention,
+# Explained", §21: low-precision operands with scaling factors). The rounding
+# step is torch's float8_e4m3fn conversion (a library primitive, pinned in the
+# tests against the e4m3 definition); everything here is on the CPU.
+
+def e4m3_values():
+    """All finite e4m3 values from the format's definition (1 sign bit, 4
+    exponent bits with bias 7, 3 mantissa bits, subnormals, no infinity,
+    exponent 15 with mantissa 7 = NaN)."""
+    vals = []
+    for e in range(16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue
+            v = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+            vals.append(v)
+    vals = sorted(set(vals))
+    return np.array(sorted(set([-v for v in vals] + vals)))
+
+
+def quantize_e4m3(x):
+    """x: [..., N, d] bf16 or float CPU tensor, per-head scale over the last
+    two dimensions. Returns (x8 as float32 values, scale [...] float32)."""
+    import torch
+    xf = x.float()
+    amax = xf.abs().amax(dim=(-1, -2))
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    x8 = (xf / scale[..., None, None]).to(torch.float8_e4m3fn)
+    return x8.float(), scale
+
+
+def fwd_fp8_dequantized(q, k, v, bias=None, scale=None, causal=False):
+    """The attention the FP8 forward approximates: fwd on the dequantized
+    scale_x * e4m3(x / scale_x) inputs (the rounding of P is the kernel's
+    approximation on top, bounded separately)."""
+    q8, sq = quantize_e4m3(q)
+    k8, sk = quantize_e4m3(k)
+    v8, sv = quantize_e4m3(v)
+    qd = q8.double() * sq.double()[..., None, None]
+    kd = k8.double() * sk.double()[..., None, None]
+    vd = v8.double() * sv.double()[..., None, None]
+    if k.shape[1] != q.shape[1]:
+        return fwd_gqa(qd, kd, vd, bias, scale=scale, causal=causal)
+    return fwd(qd, kd, vd, bias, scale=scale, causal=causal)

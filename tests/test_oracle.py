@@ -480,3 +480,63 @@ def test_varlen_oracle_sequences_do_not_interact():
     v2[:, 3:] += 100.0            # change only the last sequence's values
     o2, _ = oracle.fwd_varlen(q, k, v2, cu, cu, scale=1.0)
     np.testing.assert_array_equal(o[:, :3], o2[:, :3])
+
+
+# ---------------------------------------------------------------- e4m3 (FP8 forward)
+
+def test_e4m3_value_set_from_definition():
+    vals = oracle.e4m3_values()
+    assert len(vals) == 253                      # 2 x 127 finite codes, +0 and -0 merged
+    assert vals.max() == 448.0 and vals.min() == -448.0
+    pos = vals[vals > 0]
+    assert pos.min() == 2.0 ** -9                # smallest subnormal
+    assert 1.0 in vals and 1.125 in vals and 1.0625 not in vals
+
+
+def test_e4m3_conversion_rounds_to_nearest_even():
+    """The library conversion behind oracle.quantize_e4m3 against the format:
+    every value maps to itself, and any x in range to the nearest finite
+    e4m3 value, a tie to the one with an even mantissa."""
+    import torch
+    vals = oracle.e4m3_values()
+    t = torch.from_numpy(vals).float()
+    assert torch.equal(t.to(torch.float8_e4m3fn).float(), t)
+    # mantissa parity of each value (from its place in the ordered positive set)
+    pos = vals[vals > 0]
+    code = {v: i for i, v in enumerate(pos)}   # consecutive codes alternate mantissa parity
+    g = np.random.default_rng(5)
+    x = np.concatenate([g.uniform(-448, 448, 4000), g.uniform(-4, 4, 4000),
+                        g.uniform(-2 ** -6, 2 ** -6, 2000),
+                        (pos[:-1] + pos[1:]) / 2])              # exact midpoints (ties)
+    got = torch.from_numpy(x).float().to(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    for xi, gi in zip(x, got):
+        xa = abs(float(np.float32(xi)))
+        d = np.abs(pos - xa)
+        best = d.min()
+        cands = pos[d == best]
+        if xa < pos.min() / 2 or (xa == pos.min() / 2):
+            want = 0.0
+        elif len(cands) == 1:
+            want = cands[0]
+        else:   # tie: the even code (code 0 = 2^-9 is odd mantissa 1)
+            want = [c for c in cands if (code[c] + 1) % 2 == 0][0]
+        assert abs(gi) == want, (xi, gi, want)
+
+
+def test_quantize_e4m3_scale_and_error():
+    import torch
+    g = torch.Generator().manual_seed(3)
+    x = (torch.randn(2, 3, 50, 128, generator=g) * 3).to(torch.bfloat16)
+    x8, sc = oracle.quantize_e4m3(x)
+    xf = x.float()
+    amax = xf.abs().amax(dim=(-1, -2))
+    assert torch.equal(sc, amax / 448.0)
+    assert float(x8.abs().max()) <= 448.0
+    # the head's largest |x| lands on 448 exactly; normal values round within 2^-4 relative
+    assert torch.equal(x8.abs().amax(dim=(-1, -2)), torch.full_like(sc, 448.0))
+    rel = ((x8 * sc[..., None, None] - xf).abs() / xf.abs().clamp_min(1e-30))
+    normal = (xf / sc[..., None, None]).abs() >= 2.0 ** -6
+    assert float(rel[normal].max()) <= 2.0 ** -4 + 1e-7
+    zero = torch.zeros(1, 1, 4, 128)
+    z8, zs = oracle.quantize_e4m3(zero)
+    assert float(zs) == 1.0 and float(z8.abs().max()) == 0.0

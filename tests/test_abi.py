@@ -170,3 +170,25 @@ def test_deterministic_backward_workspace_and_validation(lib):
     for stage in (0, 4, -1):
         assert fa.fa_bwd_deterministic_stage(**dict(a, workspace_bytes=1 << 30),
                                              stage=stage) == fa.FA_ERR_INVALID_ARG
+
+
+def test_fp8_forward_workspace_and_validation(lib):
+    B, H, Hkv, Nq, Nk, d = 2, 4, 2, 300, 517, 128
+    nk16 = (Nk + 15) // 16 * 16
+    r256 = lambda x: (x + 255) // 256 * 256
+    want = (r256(4 * (B * H + 2 * B * Hkv)) + r256(B * H * Nq * d) + r256(B * Hkv * Nk * d)
+            + r256(B * Hkv * d * nk16))
+    assert fa.fa_fwd_fp8_workspace_size(B, H, Hkv, Nq, Nk, d) == want
+    assert fa.fa_fwd_fp8_workspace_size(0, H, Hkv, Nq, Nk, d) == 0
+    a = dict(q=FAKE, k=FAKE, v=FAKE, key_bias=None, o=FAKE, lse=FAKE, B=B, H=H, H_kv=Hkv, Nq=Nq,
+             Nk=Nk, d=d, scale=0.1, causal=1, workspace=FAKE, workspace_bytes=want - 1, stream=None)
+    assert fa.fa_fwd_fp8(**a) == fa.FA_ERR_INVALID_ARG           # workspace too small
+    for bad, expect in ((dict(d=64), fa.FA_ERR_UNSUPPORTED), (dict(H_kv=3), fa.FA_ERR_INVALID_ARG),
+                        (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+                        (dict(workspace=FAKE + 64), fa.FA_ERR_INVALID_ARG)):
+        b = dict(a, workspace_bytes=1 << 30)
+        b.update(bad)
+        assert fa.fa_fwd_fp8(**b) == expect, bad
+    for stage in (-1, 3):
+        assert fa.fa_fwd_fp8_stage(**dict(a, workspace_bytes=1 << 30), stage=stage) == \
+            fa.FA_ERR_INVALID_ARG

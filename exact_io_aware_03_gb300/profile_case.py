@@ -34,6 +34,8 @@ def main(argv=None):
                     help="override the workload's causal flag")
     ap.add_argument("--deterministic", action="store_true",
                     help="run fa_bwd_deterministic instead of fa_bwd")
+    ap.add_argument("--fp8", action="store_true",
+                    help="forward: run fa_fwd_fp8 (e4m3) instead of fa_fwd")
     args = ap.parse_args(argv)
 
     w = workloads.WORKLOADS[args.workload]
@@ -54,7 +56,10 @@ def main(argv=None):
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     for _ in range(args.iters):
         if args.which in ("fwd", "both"):
-            fa.fwd(q, k, v, out=o, lse=lse, **kw)
+            if args.fp8:
+                fa.fwd_fp8(q, k, v, out=o, lse=lse, **kw)
+            else:
+                fa.fwd(q, k, v, out=o, lse=lse, **kw)
         if args.which in ("bwd", "both") and w.dtype == "bf16":
             fa.bwd(q, k, v, o, lse, dO, workspace=ws, dq=dq, dk=dk, dv=dv,
                    deterministic=args.deterministic, **kw)

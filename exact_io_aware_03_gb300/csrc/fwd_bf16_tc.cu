@@ -76,19 +76,22 @@ struct FwdCfg {
   // misc: bias buffers [2 tiles][2 bufs][128] floats, then barriers
   static constexpr int OFF_BIAS = OFF_MISC;
   static constexpr int OFF_BAR = OFF_BIAS + 2 * 2 * kBN * 4;
-  static constexpr int NBAR = 2 /*q_full*/ + 4 * NS /*k/v full/empty*/ + 2 /*s_full*/ +
+  static constexpr int NBAR = 2 /*q_full*/ + 2 * NS /*kv full/empty*/ + 2 /*k0*/ + 2 /*s_full*/ +
                               2 /*p_full*/ + 2 /*o_done*/ + 4 /*bias*/ + 1 /*drain*/;
   static constexpr int OFF_SCALARS = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_SCALARS + 64;
   static constexpr int SMEM_ALLOC = BYTES + 1024;          // slack for 1024-B alignment
 };
 
+// Step i of the key loop reads V_i and K_{i+1} (PV of key tile i, S of tile
+// i+1): one barrier covers both loads and one commit releases both stages.
+// K of the first tile has its own pair.
 struct Bars {
   uint64_t* q_full;    // [2]
-  uint64_t* k_full;    // [NS]
-  uint64_t* k_empty;   // [NS]
-  uint64_t* v_full;    // [NS]
-  uint64_t* v_empty;   // [NS]
+  uint64_t* kv_full;   // [NS] V_i in V stage i%NS and K_{i+1} in K stage (i+1)%NS landed
+  uint64_t* kv_empty;  // [NS] step i's products done: V stage i%NS, K stage (i+1)%NS free
+  uint64_t* k0_full;   // K of the first key tile (K stage 0)
+  uint64_t* k0_empty;  // its S products done
   uint64_t* s_full;    // [2]
   uint64_t* p_full;    // [2]
   uint64_t* o_done;    // [2]
@@ -102,10 +105,10 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   uint64_t* b = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   Bars r;
   r.q_full = b; b += 2;
-  r.k_full = b; b += C::NS;
-  r.k_empty = b; b += C::NS;
-  r.v_full = b; b += C::NS;
-  r.v_empty = b; b += C::NS;
+  r.kv_full = b; b += C::NS;
+  r.kv_empty = b; b += C::NS;
+  r.k0_full = b; b += 1;
+  r.k0_empty = b; b += 1;
   r.s_full = b; b += 2;
   r.p_full = b; b += 2;
   r.o_done = b; b += 2;
@@ -159,11 +162,11 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
     mbar_init(&bars.q_full[0], 1);
     mbar_init(&bars.q_full[1], 1);
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&bars.k_full[s], 1);
-      mbar_init(&bars.k_empty[s], 1);
-      mbar_init(&bars.v_full[s], 1);
-      mbar_init(&bars.v_empty[s], 1);
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
     }
+    mbar_init(bars.k0_full, 1);
+    mbar_init(bars.k0_empty, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
       mbar_init(&bars.p_full[t], kBM);
@@ -253,36 +256,44 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
           tma_load_3d(q_s + t * C::TILE + c * C::SUB, &a.tm_q, c * (128 / C::EB),
                       sv.q_off + q_base + t * kBM, sv.hq, &bars.q_full[t]);
       }
-      int nk = 0, nv = 0;   // K / V fills issued
-      for (int j = lo; j < hi; ++j) {
-        const int i = j - lo, s = i % C::NS, u = i / C::NS;
-        if (u > 0 && !wait1(&bars.k_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
-        mbar_arrive_expect_tx(&bars.k_full[s], C::TILE);
+      auto load_k = [&](int j, int stage, uint64_t* bar) {
         for (int c = 0; c < C::NBOX; ++c)
-          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::SUB, &a.tm_k, c * (128 / C::EB),
-                      sv.k_off + j * kBN, sv.hk, &bars.k_full[s]);
-        ++nk;
-        if (u > 0 && !wait1(&bars.v_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
-        mbar_arrive_expect_tx(&bars.v_full[s], C::TILE);
+          tma_load_3d(smem + C::OFF_K + stage * C::TILE + c * C::SUB, &a.tm_k, c * (128 / C::EB),
+                      sv.k_off + j * kBN, sv.hk, bar);
+      };
+      auto load_v = [&](int j, int stage, uint64_t* bar) {
         if constexpr (FP8) {
           // V^T tile: 128 keys (bytes) x D rows
-          tma_load_3d(smem + C::OFF_V + s * C::TILE, &a.tm_v, j * kBN, 0, sv.hk, &bars.v_full[s]);
+          tma_load_3d(smem + C::OFF_V + stage * C::TILE, &a.tm_v, j * kBN, 0, sv.hk, bar);
         } else {
           for (int c = 0; c < C::NBOX; ++c)
-            tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::SUB, &a.tm_v, c * 64,
-                        sv.k_off + j * kBN, sv.hk, &bars.v_full[s]);
+            tma_load_3d(smem + C::OFF_V + stage * C::TILE + c * C::SUB, &a.tm_v, c * 64,
+                        sv.k_off + j * kBN, sv.hk, bar);
         }
-        ++nv;
+      };
+      mbar_arrive_expect_tx(bars.k0_full, C::TILE);
+      load_k(lo, 0, bars.k0_full);
+      int nkv = 0;   // steps whose loads were issued
+      for (int j = lo; j < hi; ++j) {
+        const int i = j - lo, s = i % C::NS, u = i / C::NS, s1 = (i + 1) % C::NS;
+        const bool next_k = j + 1 < hi;
+        // V stage s held V_{i-NS} and K stage s1 held K_{i+1-NS}: both free once
+        // step i-NS is done (for i = NS-1, K stage 0 held the first tile's K)
+        if (u > 0 && !wait1(&bars.kv_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
+        if (next_k && i + 1 == C::NS && !wait1(bars.k0_empty, 0, wc, ERR_WAIT_LOAD)) break;
+        mbar_arrive_expect_tx(&bars.kv_full[s], (next_k ? 2 : 1) * C::TILE);
+        load_v(j, s, &bars.kv_full[s]);
+        if (next_k) load_k(j + 1, s1, &bars.kv_full[s]);
+        ++nkv;
       }
       // Drain: wait (bounded, ignoring the abort flag) for the last fill of
       // every stage, so that no copy is still landing when the CTA exits.
       // In a normal run every fill has already been consumed and these
       // return at once.
       const WaitCtx wd{abort_flag, a.err, true};
-      for (int i = max(0, nk - C::NS); i < nk; ++i)
-        wait1(&bars.k_full[i % C::NS], (i / C::NS) & 1, wd, ERR_WAIT_DRAIN);
-      for (int i = max(0, nv - C::NS); i < nv; ++i)
-        wait1(&bars.v_full[i % C::NS], (i / C::NS) & 1, wd, ERR_WAIT_DRAIN);
+      wait1(bars.k0_full, 0, wd, ERR_WAIT_DRAIN);
+      for (int i = max(0, nkv - C::NS); i < nkv; ++i)
+        wait1(&bars.kv_full[i % C::NS], (i / C::NS) & 1, wd, ERR_WAIT_DRAIN);
       for (int t = 0; t < 2; ++t)
         if (hi_t[t] > lo) wait1(&bars.q_full[t], 0, wd, ERR_WAIT_DRAIN);
     }
@@ -330,7 +341,7 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t)
         if (hi_t[t] > lo) ok = wait1(&bars.q_full[t], 0, wc, ERR_WAIT_MMA);
-      if (ok) ok = wait1(&bars.k_full[0], 0, wc, ERR_WAIT_MMA);
+      if (ok) ok = wait1(bars.k0_full, 0, wc, ERR_WAIT_MMA);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
@@ -338,13 +349,13 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
             issue_s(t, 0);
             mma_commit(&bars.s_full[t]);
           }
-        mma_commit(&bars.k_empty[0]);
+        mma_commit(bars.k0_empty);
       }
       for (int j = lo; j < hi && ok; ++j) {
-        const int i = j - lo, s = i % C::NS;
-        const int i1 = i + 1, s1 = i1 % C::NS;
-        if (!wait1(&bars.v_full[s], (i / C::NS) & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
-        bool k_next = false;
+        const int i = j - lo, s = i % C::NS, s1 = (i + 1) % C::NS;
+        // V_i and K_{i+1}
+        if (!wait1(&bars.kv_full[s], (i / C::NS) & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
+        tc_fence_after();
         for (int t = 0; t < 2 && ok; ++t) {
           if (active(t, j)) {
             if (!wait1(&bars.p_full[t], i & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
@@ -353,18 +364,12 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
             mma_commit(&bars.o_done[t]);
           }
           if (j + 1 < hi && active(t, j + 1)) {
-            if (!k_next) {
-              if (!wait1(&bars.k_full[s1], (i1 / C::NS) & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
-              tc_fence_after();
-              k_next = true;
-            }
             issue_s(t, s1);
             mma_commit(&bars.s_full[t]);
           }
         }
         if (!ok) break;
-        if (j + 1 < hi) mma_commit(&bars.k_empty[s1]);
-        mma_commit(&bars.v_empty[s]);
+        mma_commit(&bars.kv_empty[s]);
       }
       // drain every MMA issued so far before TMEM is released
       mma_commit(bars.drain);

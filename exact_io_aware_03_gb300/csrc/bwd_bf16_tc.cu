@@ -65,8 +65,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
                                                       uint32_t* err) {
   // Statistics are laid out per (sequence, head) with nq_pad (a multiple of
   // 128) rows, so that every 128-row tile of them is one aligned 512-byte
-  // block; the padding rows get D = 0 and base-2 LSE = +inf (their recomputed
-  // P is exactly 0).
+  // block. They are stored in the form the main loops use them: -scale * D
+  // (dS = P o (scale * dP - scale * D) is then one fused multiply-add and a
+  // multiply, and comes out already scaled for dK and dQ) and -LSE * log2(e)
+  // (added to the base-2 score). Padding rows and rows that see no key get 0
+  // and -inf: their recomputed P is exactly 0.
   constexpr int LPR = D / 8;          // lanes per row, 8 bf16 (16 B) per lane
   constexpr int RPW = 32 / LPR;       // rows per warp step
   const int lane = threadIdx.x & 31;
@@ -103,9 +106,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 #pragma unroll
     for (int w = LPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
     if (in && li == 0) {
-      Dv[pr] = valid ? acc : 0.f;
+      Dv[pr] = valid ? -p.scale * acc : 0.f;
       const float L = valid ? lse[row] : -INFINITY;
-      lse2[pr] = (L == -INFINITY) ? INFINITY : L * kLog2e;
+      lse2[pr] = (L == -INFINITY) ? -INFINITY : -L * kLog2e;
     }
   }
 }
@@ -377,17 +380,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           // the epilogue reads dK and dV once every MMA of the CTA is done
           if (it == n - 1) mma_commit(bars.dq_full);
         } else {
-          // dK += dS^T Q (A = dS^T: K-major view of the dS boxes) ; dQ = dS K
-#pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ss(t_dk, sdesc_sw128(ds_a + (kk / 4) * C::SUB + (kk % 4) * 32, 16, 1024),
-                   sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
+          // dQ = dS K, then dK += dS^T Q (A = dS^T: K-major view of the dS
+          // boxes): dQ first, so that its read-out (which gates the next dP)
+          // starts a product earlier
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk)
             mma_ss(t_dp, sdesc_sw128(ds_a + kk * 2048, C::SUB, 1024),
                    sdesc_sw128(k_a + kk * 2048, C::SUB, 1024), id_dq, kk > 0 ? 1u : 0u);
           mma_commit(bars.dq_full);
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ss(t_dk, sdesc_sw128(ds_a + (kk / 4) * C::SUB + (kk % 4) * 32, 16, 1024),
+                   sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars.q_empty[s]);
         }
       }
@@ -409,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     constexpr int HD = D / 2;      // dQ / dK / dV columns per warpgroup
 
     // dQ of query tile `it` (TMEM lane = query row): this warpgroup's columns
-    // are read out of TMEM at once (the columns go back to the MMA warp),
-    // scaled, and reduce-added into the fp32 accumulator with TMA in boxes
+    // are read out of TMEM at once (the columns go back to the MMA warp)
+    // and reduce-added into the fp32 accumulator with TMA in boxes
     // of 32 rows x 32 columns (4 KiB, 128-byte swizzled) staged in this
     // warp's slot of the staging buffer. A TMA reduction reads its box at
     // ~25 B/clock, so a warp stages its first box right away and keeps the
@@ -426,11 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t* v = v32 + 4 * k;
-        *reinterpret_cast<uint4*>(dq_stage + lane * 128 + ((k ^ (lane & 7)) * 16)) = make_uint4(
-            __float_as_uint(__uint_as_float(v[0]) * p.scale),
-            __float_as_uint(__uint_as_float(v[1]) * p.scale),
-            __float_as_uint(__uint_as_float(v[2]) * p.scale),
-            __float_as_uint(__uint_as_float(v[3]) * p.scale));
+        *reinterpret_cast<uint4*>(dq_stage + lane * 128 + ((k ^ (lane & 7)) * 16)) =
+            make_uint4(v[0], v[1], v[2], v[3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -474,12 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tmem_ld32(lane_base + h * 64 + 32, sv + 32);
       tmem_ld_wait();
       const uint64_t sl2x2 = f2_pack(sl2, sl2), kb2 = f2_pack(kb, kb);
+      // x = S * scale * log2(e) + key bias - LSE * log2(e) (the key term is
+      // -inf for a key past the end of a ragged tile)
 #pragma unroll
       for (int e = 0; e < 64; e += 4) {
-        const float4 L4 = *reinterpret_cast<const float4*>(stl + e);
+        const float4 L4 = *reinterpret_cast<const float4*>(stl + e);   // -LSE * log2(e)
         float x[4];
-        f2_unpack(sub2(fma2(f2_pack(P[e], P[e + 1]), sl2x2, kb2), f2_pack(L4.x, L4.y)), x[0], x[1]);
-        f2_unpack(sub2(fma2(f2_pack(P[e + 2], P[e + 3]), sl2x2, kb2), f2_pack(L4.z, L4.w)), x[2],
+        f2_unpack(add2(fma2(f2_pack(P[e], P[e + 1]), sl2x2, kb2), f2_pack(L4.x, L4.y)), x[0], x[1]);
+        f2_unpack(add2(fma2(f2_pack(P[e + 2], P[e + 3]), sl2x2, kb2), f2_pack(L4.z, L4.w)), x[2],
                   x[3]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -500,10 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       mbar_arrive(bars.p_full);
       return true;
     };
-    // dS^T = P^T o (dP^T - D) of query tile `it`, into the dS boxes in shared
-    // memory (A operand of dK += dS^T Q and of dQ = dS K).
+    // dS^T = scale * P^T o (dP^T - D) of query tile `it`, into the dS boxes
+    // in shared memory (A operand of dK += dS^T Q and of dQ = dS K).
     auto compute_ds = [&](int it) -> bool {
-      const float* std_ = stat + (it & 1) * 2 * kT + kT + h * 64;
+      const float* std_ = stat + (it & 1) * 2 * kT + kT + h * 64;   // -scale * D
+      const uint64_t sc2 = f2_pack(p.scale, p.scale);
       if (!wait_warp(bars.dp_full, it & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
       // two chunks of 32 query columns, to keep the live registers low
@@ -518,12 +523,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           const float4 D4 = *reinterpret_cast<const float4*>(std_ + half * 32 + e);
           const float* Pp = P + half * 32 + e;
           float d[4];
-          f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+          f2_unpack(mul2(fma2(f2_pack(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), sc2,
                               f2_pack(D4.x, D4.y)),
                          f2_pack(Pp[0], Pp[1])),
                     d[0], d[1]);
-          f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
-                              f2_pack(D4.z, D4.w)),
+          f2_unpack(mul2(fma2(f2_pack(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
+                              sc2, f2_pack(D4.z, D4.w)),
                          f2_pack(Pp[2], Pp[3])),
                     d[2], d[3]);
           dsk[e / 2] = pack_bf16x2(d[0], d[1]);
@@ -589,7 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       const bool have = n > 0;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {   // 0: dV, 1: dK
-        const float mul = which ? p.scale : 1.f;
 #pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
           uint32_t x[32];
@@ -603,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           uint32_t pkd[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
-            pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]) * mul, __uint_as_float(x[e + 1]) * mul);
+            pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
           const int col = h * HD + c0;   // first column of these 32
           uint8_t* rowp = stage + which * C::TILE + (col / 64) * C::SUB + r * 128;
 #pragma unroll

@@ -289,9 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const float sl2 = p.scale * kLog2e;
     constexpr int HD = D / 2;                // dQ columns per warpgroup
-    // statistics of this row (padding rows: +inf and 0, so P = 0)
+    // statistics of this row, -LSE * log2(e) and -scale * D (padding rows:
+    // -inf and 0, so P = 0)
     const size_t srow = (size_t)bh * a.nq_pad + min(q0 + r, a.nq_pad - 1);
-    const float lse2 = a.lse2[srow], Drow = a.D[srow];
+    const float nlse2 = a.lse2[srow], nDrow = a.D[srow];
     // last visible key of this row / of the tile's first row
     const long lim_row = CAUSAL ? min((long)row + off, (long)Nk - 1) : (long)Nk - 1;
     const long lim_tile = CAUSAL ? min((long)q0 + off, (long)Nk - 1) : (long)Nk - 1;
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       mbar_arrive(s_free);   // the S columns may take the next tile's scores
       const bool need_mask = (long)key0 + kT - 1 > lim_tile;
       const long lim_rel = lim_row - key0 - h * 64;   // local column > lim_rel -> masked
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(nlse2, nlse2);
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
         float x0, x1;
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     auto compute_ds = [&](int i) -> bool {
       if (!wait_warp(dp_full, i & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
-      const uint64_t D2 = f2_pack(Drow, Drow);
+      const uint64_t nD2 = f2_pack(nDrow, nDrow), sc2 = f2_pack(p.scale, p.scale);
       // two chunks of 32 keys; the packed dS of chunk c goes to columns
       // [16c, 16c+16) of this warpgroup's own dP columns, already read
 #pragma unroll
@@ -373,7 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float d0, d1;
-          f2_unpack(mul2(sub2(f2_pack(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), D2),
+          // dS = scale * P o (dP - D)
+          f2_unpack(mul2(fma2(f2_pack(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), sc2,
+                              nD2),
                          f2_pack(P[half * 32 + c], P[half * 32 + c + 1])),
                     d0, d1);
           pk[c / 2] = pack_bf16x2(d0, d1);
@@ -391,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       if (!(ok = compute_ds(i))) break;
       if (i + 1 < n && !(ok = compute_p(i + 1))) break;
     }
-    // ---- dQ = scale * (dS K summed over the key tiles), bf16; rows that see
+    // ---- dQ = dS K summed over the key tiles (dS carries the scale), bf16; rows that see
     // no key get 0. Staged in the Q buffer (Q_i lives in TMEM, so the
     // buffer is free) as the 128-byte-swizzled boxes TMA uses and stored by
     // one thread with TMA; a packed sequence's ragged last tile gets plain
@@ -419,8 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
           uint32_t pkd[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
-            pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]) * p.scale,
-                                     __uint_as_float(x[e + 1]) * p.scale);
+            pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
           const int col = h * HD + c0;
           uint8_t* rowp = stage + (col / 64) * C::SUB + r * 128;
 #pragma unroll

@@ -99,8 +99,8 @@ struct BwdBf16Args {
   const uint16_t* dO;
   const float* lse;
   const float* bias;
-  float* D;            // workspace: rowsum(dO o O), [B*H][nq_pad] (0 in the padding)
-  float* lse2;         // workspace: LSE * log2(e), [B*H][nq_pad] (+inf for fully
+  float* D;            // workspace: -scale * rowsum(dO o O), [B*H][nq_pad] (0 in the padding)
+  float* lse2;         // workspace: -LSE * log2(e), [B*H][nq_pad] (-inf for fully
                        // masked rows and in the padding)
   float* dq_acc;       // workspace: fp32 dQ accumulator [B][H][Nq][d]
   uint16_t* dq;

@@ -157,8 +157,8 @@ fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, const floa
                          int num_splits, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: D = rowsum(dO o O) and the LSE
- * rescaled to base 2, each fp32 [B*H][Nq rounded up to a multiple of 128],
+ * Bytes of device workspace fa_bwd needs: -scale * D with D = rowsum(dO o O),
+ * and -LSE rescaled to base 2, each fp32 [B*H][Nq rounded up to a multiple of 128],
  * and an fp32 dQ accumulator [B,H,Nq,d], each starting on a 256-byte boundary.
  * Returns 0 for invalid sizes.
  */
@@ -188,7 +188,7 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
  * validation; calling them in this order on one stream is equivalent to
  * fa_bwd ("flash-attention", Part VII: a preprocess launch, then the main
  * backward launch):
- *   fa_bwd_preprocess   D = rowsum(dO o O), base-2 LSE, zeroed dQ accumulator
+ *   fa_bwd_preprocess   -scale * rowsum(dO o O), -base-2 LSE, zeroed dQ accumulator
  *                       (reads o, lse, dO; writes the workspace);
  *   fa_bwd_main         recompute P per tile, dK and dV (written to dk, dv),
  *                       dQ reduced into the workspace accumulator;

@@ -151,10 +151,10 @@ struct BwdBars {
   uint64_t* do_empty;  // [ND]
   uint64_t* s_full;    // S^T done
   uint64_t* dp_full;   // dP^T done
-  uint64_t* p_full;    // P^T in TMEM (128 arrivals)
-  uint64_t* ds_full;   // dS^T in TMEM + smem (128 arrivals)
+  uint64_t* p_full;    // P^T in TMEM (one arrival per compute warp)
+  uint64_t* ds_full;   // dS^T in TMEM + smem (one arrival per compute warp)
   uint64_t* dq_full;   // dQ_i done (and everything before it); DET: the last dK done
-  uint64_t* dq_empty;  // dQ_i read out of TMEM (128 arrivals)
+  uint64_t* dq_empty;  // dQ_i read out of TMEM (one arrival per compute warp)
   uint64_t* drain;
 };
 
@@ -240,10 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     }
     mbar_init(bars.s_full, 1);
     mbar_init(bars.dp_full, 1);
-    mbar_init(bars.p_full, 2 * kT);
-    mbar_init(bars.ds_full, 2 * kT);
+    mbar_init(bars.p_full, 2 * kT / 32);    // one arrival per compute warp
+    mbar_init(bars.ds_full, 2 * kT / 32);
     mbar_init(bars.dq_full, 1);
-    mbar_init(bars.dq_empty, 2 * kT);
+    mbar_init(bars.dq_empty, 2 * kT / 32);
     mbar_init(bars.drain, 1);
     *abort_flag = (smem_u32(smem) & 1023u) != 0;
     *any_key = 0;
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       if constexpr (HD > 32) tmem_ld32(lane_base + 128 + h * HD + 32, dq_hold);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(bars.dq_empty);
+      mbar_arrive_warp(bars.dq_empty);
       hold_row0 = sv.q_off + q_row0(it) + (warp % 4) * 32;
       hold_qc = q_coord(q_head(it));
       stage_box(x, h * HD, hold_row0, hold_qc);
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bars.p_full);
+      mbar_arrive_warp(bars.p_full);
       return true;
     };
     // dS^T = scale * P^T o (dP^T - D) of query tile `it`, into the dS boxes
@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(bars.ds_full);
+      mbar_arrive_warp(bars.ds_full);
       return true;
     };
 

@@ -83,12 +83,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   uint64_t* v_full = bb;   bb += C::NSV;
   uint64_t* v_empty = bb;  bb += C::NSV;
   uint64_t* s_full = bb;   bb += 1;   // S done
-  uint64_t* s_free = bb;   bb += 1;   // S read by both warpgroups (256 arrivals)
-  uint64_t* qt_ready = bb; bb += 1;   // Q_i, dO_i copied into TMEM (256 arrivals)
+  uint64_t* s_free = bb;   bb += 1;   // S read by both warpgroups (one arrival per warp)
+  uint64_t* qt_ready = bb; bb += 1;   // Q_i, dO_i copied into TMEM (one arrival per warp)
   uint64_t* dp_full = bb;  bb += 1;
-  uint64_t* ds_full = bb;  bb += 1;   // dS in TMEM (256 arrivals)
+  uint64_t* ds_full = bb;  bb += 1;   // dS in TMEM (one arrival per warp)
   uint64_t* dq_full = bb;  bb += 1;   // every dQ product done
-  uint64_t* bias_rdy = bb; bb += 4;   // [warpgroup][buffer], 128 arrivals
+  uint64_t* bias_rdy = bb; bb += 4;   // [warpgroup][buffer], one arrival per warp
   uint64_t* drain = bb;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_SCALARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SCALARS + 4);
@@ -127,12 +127,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       mbar_init(&v_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 2 * kT);
-    mbar_init(qt_ready, 2 * kT);
+    mbar_init(s_free, 2 * kT / 32);   // one arrival per compute warp
+    mbar_init(qt_ready, 2 * kT / 32);
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 2 * kT);
+    mbar_init(ds_full, 2 * kT / 32);
     mbar_init(dq_full, 1);
-    for (int t = 0; t < 4; ++t) mbar_init(&bias_rdy[t], kT);
+    for (int t = 0; t < 4; ++t) mbar_init(&bias_rdy[t], kT / 32);
     mbar_init(drain, 1);
     *abort_flag = (smem_u32(smem) & 1023u) != 0;
     *key_lo_s = Nk;
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(qt_ready);
+      mbar_arrive_warp(qt_ready);
       return true;
     };
     float P[64];
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       if (BIAS) {
         float* w = bias_buf + (h * 2 + (i & 1)) * kT;
         w[r] = key0 + r < Nk ? bias_row[key0 + r] * kLog2e : -INFINITY;
-        mbar_arrive(&bias_rdy[h * 2 + (i & 1)]);
+        mbar_arrive_warp(&bias_rdy[h * 2 + (i & 1)]);
         if (!wait_warp(&bias_rdy[h * 2 + (i & 1)], (i >> 1) & 1, wc, ERR_WAIT_SOFTMAX))
           return false;
       }
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       tmem_ld32(lane_base + h * 64 + 32, su + 32);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(s_free);   // the S columns may take the next tile's scores
+      mbar_arrive_warp(s_free);   // the S columns may take the next tile's scores
       const bool need_mask = (long)key0 + kT - 1 > lim_tile;
       const long lim_rel = lim_row - key0 - h * 64;   // local column > lim_rel -> masked
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(nlse2, nlse2);
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(ds_full);
+      mbar_arrive_warp(ds_full);
       return true;
     };
     bool ok = n == 0 || (copy_q_do() && compute_p(0));

@@ -169,10 +169,10 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
     mbar_init(bars.k0_empty, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
-      mbar_init(&bars.p_full[t], kBM);
+      mbar_init(&bars.p_full[t], kBM / 32);   // one arrival per softmax warp
       mbar_init(&bars.o_done[t], 1);
-      mbar_init(&bars.bias_rdy[2 * t + 0], kBM);
-      mbar_init(&bars.bias_rdy[2 * t + 1], kBM);
+      mbar_init(&bars.bias_rdy[2 * t + 0], kBM / 32);
+      mbar_init(&bars.bias_rdy[2 * t + 1], kBM / 32);
     }
     mbar_init(bars.drain, 1);
     *abort_flag = 0;
@@ -400,7 +400,7 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
         float* bb = bias_buf + (t * 2 + (i & 1)) * kBN;
         const int kj = key0 + r;
         bb[r] = kj < Nk ? bias_row[kj] * kLog2e : -INFINITY;
-        mbar_arrive(&bars.bias_rdy[t * 2 + (i & 1)]);
+        mbar_arrive_warp(&bars.bias_rdy[t * 2 + (i & 1)]);
         if (!wait_warp(&bars.bias_rdy[t * 2 + (i & 1)], (i >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) break;
       }
       if (!wait_warp(&bars.s_full[t], i & 1, wc, ERR_WAIT_SOFTMAX)) break;
@@ -505,7 +505,7 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars.p_full[t]);
+      mbar_arrive_warp(&bars.p_full[t]);
     }
     // ---- epilogue: O = O_acc / l (bf16), LSE = ln2 * (m + log2 l)
     const bool completed = (i == n_t);

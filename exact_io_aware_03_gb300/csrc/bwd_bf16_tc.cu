@@ -155,7 +155,7 @@ struct BwdBars {
   uint64_t* ds_full;   // dS^T in TMEM + smem (one arrival per compute warp)
   uint64_t* dq_full;   // dQ_i done (and everything before it); DET: the last dK done
   uint64_t* dq_empty;  // dQ_i read out of TMEM (one arrival per compute warp)
-  uint64_t* drain;
+  uint64_t* drain;     // every MMA of the CTA done (the MMA warp's final commit)
 };
 
 
@@ -572,11 +572,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       if (!DET && !(ok = dq_readout(it))) break;   // the last one: every MMA of this CTA is done
     }
     if (!DET) {
-      if (ok && it == n && n > 0) dq_finish();
+      if (ok && it == n && n > 0) {
+        dq_finish();
+        // dK of the last tile is issued after its dQ: wait for every MMA of
+        // the CTA (the MMA warp's final commit) before reading dK and dV
+        ok = wait_warp(bars.drain, 0, wc, ERR_WAIT_EPILOGUE);
+        tc_fence_after();
+      }
       if (lane == 0) bulk_wait_group0();   // reductions complete before the CTA exits
       __syncwarp();
     } else if (ok && it == n && n > 0) {
-      // (the non-deterministic path waited for this in the last dQ read-out)
+      // dq_full follows the last dK here
       ok = wait_warp(bars.dq_full, 0, wc, ERR_WAIT_EPILOGUE);
       tc_fence_after();
     }

@@ -138,13 +138,14 @@ struct BwdCfg {
   // per Q stage: base-2 LSE [128] then D [128] of the tile's rows (TMA)
   static constexpr int OFF_STAT = OFF_DS + (DET ? 0 : kT * kT * 2);
   static constexpr int OFF_BAR = OFF_STAT + 2 * 2 * kT * 4;
-  static constexpr int NBAR = 1 + 2 + 2 + 2 * ND + 1 + 1 + 1 + 1 + 1 + 1 + 1;
+  static constexpr int NBAR = 2 + 2 + 2 + 2 * ND + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 2 + 2 + 1;
   static constexpr int OFF_SCALARS = OFF_BAR + NBAR * 8;
-  static constexpr int BYTES = OFF_SCALARS + 32;
+  static constexpr int BYTES = OFF_SCALARS + 16 + 2 * 48;   // flags, then the work-item ring
 };
 
 struct BwdBars {
-  uint64_t* kv_full;   // [1]
+  uint64_t* kv_full;   // K, V of the current item landed
+  uint64_t* kv_empty;  // every MMA of an item done (its K/V free, dK and dV final)
   uint64_t* q_full;    // [2]  Q_i and its base-2 LSE and D of a stage
   uint64_t* q_empty;   // [2]
   uint64_t* do_full;   // [ND] dO_i
@@ -156,9 +157,94 @@ struct BwdBars {
   uint64_t* dq_full;   // dQ_i done (and everything before it); DET: the last dK done
   uint64_t* dq_empty;  // dQ_i read out of TMEM (one arrival per compute warp)
   uint64_t* drain;     // every MMA of the CTA done (the MMA warp's final commit)
+  uint64_t* sched_full;    // [2] work-item ring: item index written
+  uint64_t* sched_empty;   // [2] read by the MMA thread and every compute warp
+  uint64_t* cw;        // barrier of the compute warps (one arrival per warp)
 };
 
 
+// ------------------------------------------------------------------ work items
+// A work item is one (key/value head, key tile). Items are numbered in this
+// order: heads in groups of a.head_group whose Q, dO (and dQ accumulator)
+// stay in L2 together; within a group, key tile by key tile over the group's
+// heads, low key tiles (the most query tiles under a causal mask) first, so
+// that the last items to start are the short ones.
+struct BwdItem {
+  int b, h_q0, grp, key0, Nq, Nk, i0, nqh;
+  int n;      // query-tile steps: every query head of the group x query tiles [i0, n_qt)
+  long off;   // Nk - Nq: bottom-right causal alignment
+  SeqView sv;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ BwdItem bwd_item(const BwdBf16Args& a, int w) {
+  const Problem& p = a.p;
+  BwdItem t;
+  const int n_kt = (p.Nk + kT - 1) / kT;
+  const int BHkv = p.B * p.Hkv;
+  const int G = a.head_group;
+  const int g0 = (int)(w / ((long)G * n_kt)) * G;
+  const int gsz = min(G, BHkv - g0);
+  const int rr = (int)(w - (long)g0 * n_kt);
+  const int bh_kv = g0 + rr % gsz;
+  t.b = bh_kv / p.Hkv;
+  t.grp = p.H / p.Hkv;
+  t.h_q0 = (bh_kv % p.Hkv) * t.grp;   // first query head of the group
+  // rows and lengths of this sequence (keys and queries numbered from 0 in it)
+  t.sv = seq_view(p, t.b, t.h_q0);
+  t.Nq = t.sv.len_q;
+  t.Nk = t.sv.len_k;
+  t.key0 = (rr / gsz) * kT;
+  t.off = (long)t.Nk - t.Nq;
+  // query tiles [i0, n_qt) can see this key tile
+  const int n_qt = (t.Nq + kT - 1) / kT;
+  t.i0 = 0;
+  if (CAUSAL) {
+    // smallest i with i*128 + 127 + off >= key0
+    const long need = (long)t.key0 - t.off - (kT - 1);
+    t.i0 = need <= 0 ? 0 : (int)min((long)n_qt, (need + kT - 1) / kT);
+  }
+  t.nqh = n_qt - t.i0;
+  t.n = t.key0 < t.Nk ? max(0, t.nqh) * t.grp : 0;
+  return t;
+}
+
+// A slot of the work-item ring in shared memory: the item and what the loops
+// of the MMA and P/dS warps need of it, decoded once by the TMA warp.
+struct BwdSlot {
+  int w;          // item index; -1: no more items
+  int n;          // query-tile steps (0: nothing to compute, dK = dV = 0)
+  int i0, nqh;    // query tiles [i0, i0 + nqh) of each query head (nqh >= 1)
+  int off;        // Nk - Nq of the sequence
+  int key0;       // first key of the tile
+  int qc0;        // coordinate of the group's first query head in q / dO / dq
+  int q_off;      // first row of the sequence
+  int nk;         // keys of the sequence
+  int bias_row;   // b * Nk: the sequence's row of the key bias
+  int g0;         // global index of the item's first query-tile step
+  int kph;        // ordinal of the item among the CTA's items with n > 0
+};
+
+// Warp-collective: whether any key of the item's tile has a finite bias (a
+// tile whose keys are all masked out contributes nothing: dK = dV = 0).
+__device__ __forceinline__ bool bwd_item_any_key(const BwdBf16Args& a, const BwdItem& t) {
+  bool any = false;
+#pragma unroll
+  for (int m = 0; m < kT / 32; ++m) {
+    const int key = t.key0 + m * 32 + (int)lane_id();
+    if (key < t.Nk && a.bias[(size_t)t.b * t.Nk + key] * kLog2e != -INFINITY) any = true;
+  }
+  return __any_sync(0xffffffffu, any);
+}
+
+// The main backward kernel. The non-deterministic form is persistent: one
+// CTA per SM takes work items in order from a counter in the workspace
+// (the TMA warp fetches them and passes them to the MMA warp and the P/dS
+// warps through a two-slot ring in shared memory), and every barrier phase
+// and ring stage runs on across items. So the next item's K/V and first Q,
+// dO tiles load, and its first S^T and dP^T products run, while the P/dS
+// warps write out the previous item's dK and dV. The deterministic form
+// (dS^T through TMEM, no dQ) takes one item per CTA, the CTA's index.
 template <int D, bool CAUSAL, bool BIAS, bool DET>
 __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdBf16Args a) {
   using C = BwdCfg<D, DET>;
@@ -170,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   BwdBars bars;
   bars.kv_full = bb; bb += 1;
+  bars.kv_empty = bb; bb += 1;
   bars.q_full = bb; bb += 2;
   bars.q_empty = bb; bb += 2;
   bars.do_full = bb; bb += C::ND;
@@ -180,59 +267,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   bars.ds_full = bb; bb += 1;
   bars.dq_full = bb; bb += 1;
   bars.dq_empty = bb; bb += 1;
-  bars.drain = bb;
+  bars.drain = bb; bb += 1;
+  bars.sched_full = bb; bb += 2;
+  bars.sched_empty = bb; bb += 2;
+  bars.cw = bb;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_SCALARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SCALARS + 4);
-  int* any_key = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 8);
+  volatile BwdSlot* slots = reinterpret_cast<volatile BwdSlot*>(smem + C::OFF_SCALARS + 16);   // [2]
   const WaitCtx wc{abort_flag, a.err};
-
-  // One CTA per (key/value head, key tile). With grouped heads it walks the
-  // query tiles of every query head of its group, so dK and dV of the shared
-  // head accumulate over the whole group in TMEM.
-  // Order: heads in groups of a.head_group whose Q, dO (and dQ accumulator)
-  // stay in L2 together; within a group, key tile by key tile over the
-  // group's heads, low key tiles (the most query tiles under a causal mask)
-  // first, so that the last CTAs to start are the short ones.
-  const int n_kt = (p.Nk + kT - 1) / kT;
-  const int BHkv = p.B * p.Hkv;
-  const int G = a.head_group;
-  const int grp_i = (int)(blockIdx.x / ((long)G * n_kt));
-  const int g0 = grp_i * G;
-  const int gsz = min(G, BHkv - g0);
-  const int rr = (int)(blockIdx.x - (long)g0 * n_kt);
-  const int bh_kv = g0 + rr % gsz;
-  const int jt = rr / gsz;
-  const int b = bh_kv / p.Hkv;
-  const int grp = p.H / p.Hkv;
-  const int h_q0 = (bh_kv % p.Hkv) * grp;   // first query head of the group
-  // rows and lengths of this sequence (keys and queries numbered from 0 in it)
-  const SeqView sv = seq_view(p, b, h_q0);
-  const int Nq = sv.len_q, Nk = sv.len_k;
-  const int key0 = jt * kT;
-  const long off = (long)Nk - Nq;
-
-  // ---- query tiles [i0, i1) that can see this key tile
-  const int n_qt = (Nq + kT - 1) / kT;
-  int i0 = 0;
-  if (CAUSAL) {
-    // smallest i with i*128 + 127 + off >= key0
-    const long need = (long)key0 - off - (kT - 1);
-    i0 = need <= 0 ? 0 : (int)min((long)n_qt, (need + kT - 1) / kT);
-  }
-  const int i1 = n_qt;
-  const int nqh = i1 - i0;   // query tiles per query head
-  // query head and tile of step `it` of this CTA
-  // query head (within the batch) of step `it`, and its coordinate in q/dO/dq
-  auto q_head = [&](int it) { return h_q0 + it / max(nqh, 1); };
-  auto q_coord = [&](int h) { return p.cu_q ? h : b * p.H + h; };
-  auto q_row0 = [&](int it) { return (i0 + it % max(nqh, 1)) * kT; };
+  const int n_items = p.B * p.Hkv * ((p.Nk + kT - 1) / kT);
 
   if (threadIdx.x == 0) {
     if ((smem_u32(smem) & 1023u) != 0) atomicOr(a.err, ERR_WAIT_DRAIN);   // layout invariant
     mbar_init(bars.kv_full, 1);
+    mbar_init(bars.kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.sched_full[s], 1);
+      mbar_init(&bars.sched_empty[s], 1 + 2 * kT / 32);   // the MMA thread + each compute warp
     }
     for (int s = 0; s < C::ND; ++s) {
       mbar_init(&bars.do_full[s], 1);
@@ -245,157 +298,227 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     mbar_init(bars.dq_full, 1);
     mbar_init(bars.dq_empty, 2 * kT / 32);
     mbar_init(bars.drain, 1);
+    mbar_init(bars.cw, 2 * kT / 32);
     *abort_flag = (smem_u32(smem) & 1023u) != 0;
-    *any_key = 0;
     fence_mbar_init();
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  __syncthreads();
-  // per-key bias (log2 domain); keys past Nk are masked
-  float kb = -INFINITY;
-  if (warp < 8) {
-    const int key = key0 + (threadIdx.x & 127);
-    if (key < Nk) kb = BIAS ? a.bias[(size_t)b * Nk + key] * kLog2e : 0.f;
-    if (kb != -INFINITY) *any_key = 1;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n = (*any_key && !*abort_flag) ? max(0, nqh) * grp : 0;
+
+  // query head (within the batch) and first row of step `lt` of item t, and
+  // the head's coordinate in q/dO/dq
+  auto q_head = [&](const BwdItem& t, int lt) { return t.h_q0 + lt / max(t.nqh, 1); };
+  auto q_coord = [&](const BwdItem& t, int h) { return p.cu_q ? h : t.b * p.H + h; };
+  auto q_row0 = [&](const BwdItem& t, int lt) { return (t.i0 + lt % max(t.nqh, 1)) * kT; };
 
   if (warp == 8) {
-    // ================================================================ TMA producer
-    if (lane == 0 && n > 0) {
-      mbar_arrive_expect_tx(bars.kv_full, 2 * C::TILE);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, sv.k_off + key0, sv.hk,
-                    bars.kv_full);
-        tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, sv.k_off + key0, sv.hk,
-                    bars.kv_full);
+    // ================================================================ TMA producer + scheduler
+    int g = 0, kph = 0;     // query-tile steps / non-empty items so far
+    int nq = 0, nd = 0, nkv = 0;   // Q / dO / K,V fills issued
+    bool ok = true;
+    for (int u = 0; ok; ++u) {
+      int w;
+      if (DET) {
+        w = u == 0 ? (int)blockIdx.x : -1;
+      } else {
+        w = lane == 0 ? atomicAdd(a.sched, 1) : 0;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (w >= n_items) w = -1;
       }
-      int nq = 0, nd = 0;   // Q / dO fills issued
-      for (int it = 0; it < n; ++it) {
-        const int s = it & 1, u = it >> 1;
-        const int q0 = q_row0(it), hq = q_head(it);
-        if (u > 0 && !wait1(&bars.q_empty[s], (u - 1) & 1, wc, ERR_WAIT_LOAD)) break;
-        mbar_arrive_expect_tx(&bars.q_full[s], C::TILE + 2 * kT * 4);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * C::SUB, &a.tm_q, c * 64, sv.q_off + q0,
-                      q_coord(hq), &bars.q_full[s]);
-        float* st = reinterpret_cast<float*>(smem + C::OFF_STAT) + s * 2 * kT;
-        const size_t srow = ((size_t)b * p.H + hq) * a.nq_pad + q0;
-        bulk_load_1d(st, a.lse2 + srow, kT * 4, &bars.q_full[s]);
-        bulk_load_1d(st + kT, a.D + srow, kT * 4, &bars.q_full[s]);
-        ++nq;
-        // dO stage sd may be refilled once dV of its previous tile is done
-        const int sd = it % C::ND, ud = it / C::ND;
-        if (ud > 0 && !wait1(&bars.do_empty[sd], (ud - 1) & 1, wc, ERR_WAIT_LOAD)) break;
-        mbar_arrive_expect_tx(&bars.do_full[sd], C::TILE);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_DO + sd * C::TILE + c * C::SUB, &a.tm_do, c * 64,
-                      sv.q_off + q0, q_coord(hq), &bars.do_full[sd]);
-        ++nd;
+      BwdItem t;
+      int n = 0;
+      if (w >= 0) {
+        t = bwd_item<CAUSAL>(a, w);
+        n = (!BIAS || bwd_item_any_key(a, t)) ? t.n : 0;
       }
+      if (lane == 0) {
+        // slot u & 1 is free once item u - 2 is done with it
+        if (u >= 2 && !wait1(&bars.sched_empty[u & 1], ((u >> 1) - 1) & 1, wc, ERR_WAIT_LOAD)) ok = false;
+        if (ok) {
+          volatile BwdSlot* sl = slots + (u & 1);
+          sl->w = w;
+          if (w >= 0) {
+            sl->n = n;
+            sl->i0 = t.i0;
+            sl->nqh = max(t.nqh, 1);
+            sl->off = (int)t.off;
+            sl->key0 = t.key0;
+            sl->qc0 = p.cu_q ? t.h_q0 : t.b * p.H + t.h_q0;
+            sl->q_off = t.sv.q_off;
+            sl->nk = t.Nk;
+            sl->bias_row = t.b * t.Nk;
+            sl->g0 = g;
+            sl->kph = kph;
+          }
+          mbar_arrive(&bars.sched_full[u & 1]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok || w < 0) break;
+      if (n == 0) continue;
+      if (lane == 0 && !*abort_flag) {
+        // K and V of the previous item are free once all of its MMAs are done
+        if (kph > 0 && !wait1(bars.kv_empty, (kph - 1) & 1, wc, ERR_WAIT_LOAD)) ok = false;
+        if (ok) {
+          mbar_arrive_expect_tx(bars.kv_full, 2 * C::TILE);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, t.sv.k_off + t.key0, t.sv.hk,
+                        bars.kv_full);
+            tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, t.sv.k_off + t.key0, t.sv.hk,
+                        bars.kv_full);
+          }
+          ++nkv;
+        }
+        for (int lt = 0; lt < n && ok; ++lt) {
+          const int gi = g + lt, s = gi & 1, uq = gi >> 1;
+          const int q0 = q_row0(t, lt), hq = q_head(t, lt);
+          if (uq > 0 && !wait1(&bars.q_empty[s], (uq - 1) & 1, wc, ERR_WAIT_LOAD)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars.q_full[s], C::TILE + 2 * kT * 4);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * C::SUB, &a.tm_q, c * 64,
+                        t.sv.q_off + q0, q_coord(t, hq), &bars.q_full[s]);
+          float* st = reinterpret_cast<float*>(smem + C::OFF_STAT) + s * 2 * kT;
+          const size_t srow = ((size_t)t.b * p.H + hq) * a.nq_pad + q0;
+          bulk_load_1d(st, a.lse2 + srow, kT * 4, &bars.q_full[s]);
+          bulk_load_1d(st + kT, a.D + srow, kT * 4, &bars.q_full[s]);
+          ++nq;
+          // dO stage sd may be refilled once dV of its previous tile is done
+          const int sd = gi % C::ND, ud = gi / C::ND;
+          if (ud > 0 && !wait1(&bars.do_empty[sd], (ud - 1) & 1, wc, ERR_WAIT_LOAD)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars.do_full[sd], C::TILE);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::OFF_DO + sd * C::TILE + c * C::SUB, &a.tm_do, c * 64,
+                        t.sv.q_off + q0, q_coord(t, hq), &bars.do_full[sd]);
+          ++nd;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      g += n;
+      ++kph;
+    }
+    if (lane == 0) {
+      // Drain: wait (bounded, ignoring the abort flag) for the last fill of
+      // every buffer, so that no copy is still landing when the CTA exits.
       const WaitCtx wd{abort_flag, a.err, true};
-      wait1(bars.kv_full, 0, wd, ERR_WAIT_DRAIN);
-      for (int it = max(0, nq - 2); it < nq; ++it)
-        wait1(&bars.q_full[it & 1], (it >> 1) & 1, wd, ERR_WAIT_DRAIN);
-      for (int it = max(0, nd - C::ND); it < nd; ++it)
-        wait1(&bars.do_full[it % C::ND], (it / C::ND) & 1, wd, ERR_WAIT_DRAIN);
+      if (nkv > 0) wait1(bars.kv_full, (nkv - 1) & 1, wd, ERR_WAIT_DRAIN);
+      for (int i = max(0, nq - 2); i < nq; ++i) wait1(&bars.q_full[i & 1], (i >> 1) & 1, wd, ERR_WAIT_DRAIN);
+      for (int i = max(0, nd - C::ND); i < nd; ++i)
+        wait1(&bars.do_full[i % C::ND], (i / C::ND) & 1, wd, ERR_WAIT_DRAIN);
     }
   } else if (warp == 9) {
     // ================================================================ MMA issuer
-    if (lane == 0 && n > 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);    // S^T, dP^T
-      constexpr uint32_t id_acc = idesc_bf16_f32(kT, D, false, true);    // dV, dK (A K-major)
-      constexpr uint32_t id_dq = idesc_bf16_f32(kT, D, true, true);      // dQ (A = dS, MN-major)
-      const uint32_t k_a = smem_u32(smem + C::OFF_K), v_a = smem_u32(smem + C::OFF_V);
-      const uint32_t ds_a = smem_u32(smem + C::OFF_DS);
-      const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
-      // S^T = K Q^T for query tile `it` (both K-major, 128-byte rows per box)
-      auto issue_s = [&](int it) {
-        const uint32_t q_a = smem_u32(smem + C::OFF_Q + (it & 1) * C::TILE);
+    constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);    // S^T, dP^T
+    constexpr uint32_t id_acc = idesc_bf16_f32(kT, D, false, true);    // dV, dK (A K-major)
+    constexpr uint32_t id_dq = idesc_bf16_f32(kT, D, true, true);      // dQ (A = dS, MN-major)
+    const uint32_t k_a = smem_u32(smem + C::OFF_K), v_a = smem_u32(smem + C::OFF_V);
+    const uint32_t ds_a = smem_u32(smem + C::OFF_DS);
+    const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
+    // S^T = K Q^T for global step gi (both K-major, 128-byte rows per box)
+    auto issue_s = [&](int gi) {
+      const uint32_t q_a = smem_u32(smem + C::OFF_Q + (gi & 1) * C::TILE);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
-          mma_ss(t_s, sdesc_sw128(k_a + o, 16, 1024), sdesc_sw128(q_a + o, 16, 1024), id_s, kk > 0);
-        }
-        mma_commit(bars.s_full);
-      };
-      // Issue order per query tile i:  dP(i) [after dQ(i-1) left TMEM],
-      // dV(i) [after P(i)], S(i+1) [the S columns are free once dV(i) has
-      // read P(i)], dK(i), dQ(i) [after dS(i)]. S(i+1) and the softmax of
-      // tile i+1 thus overlap dK(i) and dQ(i).
-      bool ok = wait1(bars.kv_full, 0, wc, ERR_WAIT_MMA);
-      if (ok && (ok = wait1(&bars.q_full[0], 0, wc, ERR_WAIT_MMA))) {
-        tc_fence_after();
-        issue_s(0);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
+        mma_ss(t_s, sdesc_sw128(k_a + o, 16, 1024), sdesc_sw128(q_a + o, 16, 1024), id_s, kk > 0);
       }
-      for (int it = 0; it < n && ok; ++it) {
-        const int s = it & 1, sd = it % C::ND;
-        const uint32_t q_a = smem_u32(smem + C::OFF_Q + s * C::TILE);
-        const uint32_t do_a = smem_u32(smem + C::OFF_DO + sd * C::TILE);
-        // dP^T = V dO^T, once dQ of the previous tile has left TMEM (DET: the
-        // dS^T of the previous tile in these columns was read by dK, an
-        // earlier MMA)
-        if (!DET && it > 0 && !(ok = wait1(bars.dq_empty, (it - 1) & 1, wc, ERR_WAIT_MMA))) break;
-        if (!(ok = wait1(&bars.do_full[sd], (it / C::ND) & 1, wc, ERR_WAIT_MMA))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
-          mma_ss(t_dp, sdesc_sw128(v_a + o, 16, 1024), sdesc_sw128(do_a + o, 16, 1024), id_s,
-                 kk > 0);
+      mma_commit(bars.s_full);
+    };
+    int g = 0, kph = 0;
+    bool ok = true, issued = false;
+    for (int u = 0; ok; ++u) {
+      if (!wait_warp(&bars.sched_full[u & 1], (u >> 1) & 1, wc, ERR_WAIT_LOAD)) break;
+      const int w = slots[u & 1].w, n = slots[u & 1].n;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.sched_empty[u & 1]);
+      if (w < 0) break;
+      if (n == 0) continue;
+      if (lane == 0) {
+        // Issue order per query tile i:  dP(i) [after dQ(i-1) left TMEM],
+        // dV(i) [after P(i)], S(i+1) [the S columns are free once dV(i) has
+        // read P(i)], dQ(i) and dK(i) [after dS(i)]. S(i+1) and the softmax
+        // of tile i+1 thus overlap dQ(i) and dK(i). The first dV and dK of
+        // an item start from zero: the P/dS warps arrive on P of the item's
+        // first tile only after they have read the previous item's dK, dV.
+        ok = !*abort_flag && wait1(bars.kv_full, kph & 1, wc, ERR_WAIT_MMA) &&
+             wait1(&bars.q_full[g & 1], (g >> 1) & 1, wc, ERR_WAIT_MMA);
+        if (ok) {
+          tc_fence_after();
+          issue_s(g);
+          issued = true;
         }
-        mma_commit(bars.dp_full);
-        // dV(it) and S(it+1) are issued back to back once both can go: a wait
-        // between two products would let the MMA queue run dry
-        if (!(ok = wait1(bars.p_full, it & 1, wc, ERR_WAIT_MMA))) break;
-        if (it + 1 < n &&
-            !(ok = wait1(&bars.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
-          break;
-        tc_fence_after();
-        // dV += P^T dO  (P^T packed bf16: query columns [0,64) in TMEM columns
-        // [0,32), [64,128) in [64,96))
+        for (int lt = 0; lt < n && ok; ++lt) {
+          const int gi = g + lt, s = gi & 1, sd = gi % C::ND;
+          const uint32_t q_a = smem_u32(smem + C::OFF_Q + s * C::TILE);
+          const uint32_t do_a = smem_u32(smem + C::OFF_DO + sd * C::TILE);
+          // dP^T = V dO^T, once dQ of the previous tile has left TMEM (DET: the
+          // dS^T of the previous tile in these columns was read by dK, an
+          // earlier MMA)
+          if (!DET && gi > 0 && !(ok = wait1(bars.dq_empty, (gi - 1) & 1, wc, ERR_WAIT_MMA))) break;
+          if (!(ok = wait1(&bars.do_full[sd], (gi / C::ND) & 1, wc, ERR_WAIT_MMA))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8,
-                 sdesc_sw128(do_a + kk * 2048, C::SUB, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.do_empty[sd]);   // dV is the last reader of dO(it)
-        if (it + 1 < n) issue_s(it + 1);
-        if (!(ok = wait1(bars.ds_full, it & 1, wc, ERR_WAIT_MMA))) break;
-        tc_fence_after();
-        if constexpr (DET) {
-          // dK += dS^T Q with dS^T packed in TMEM like P^T (in the dP^T columns)
-#pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(t_dk, t_dp + (kk / 4) * 64 + (kk % 4) * 8,
-                   sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.q_empty[s]);
-          // the epilogue reads dK and dV once every MMA of the CTA is done
-          if (it == n - 1) mma_commit(bars.dq_full);
-        } else {
-          // dQ = dS K, then dK += dS^T Q (A = dS^T: K-major view of the dS
-          // boxes): dQ first, so that its read-out (which gates the next dP)
-          // starts a product earlier
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
+            mma_ss(t_dp, sdesc_sw128(v_a + o, 16, 1024), sdesc_sw128(do_a + o, 16, 1024), id_s,
+                   kk > 0);
+          }
+          mma_commit(bars.dp_full);
+          // dV(i) and S(i+1) are issued back to back once both can go: a wait
+          // between two products would let the MMA queue run dry
+          if (!(ok = wait1(bars.p_full, gi & 1, wc, ERR_WAIT_MMA))) break;
+          if (lt + 1 < n &&
+              !(ok = wait1(&bars.q_full[(gi + 1) & 1], ((gi + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
+            break;
+          tc_fence_after();
+          // dV += P^T dO  (P^T packed bf16: query columns [0,64) in TMEM columns
+          // [0,32), [64,128) in [64,96))
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ss(t_dp, sdesc_sw128(ds_a + kk * 2048, C::SUB, 1024),
-                   sdesc_sw128(k_a + kk * 2048, C::SUB, 1024), id_dq, kk > 0 ? 1u : 0u);
-          mma_commit(bars.dq_full);
+            mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8,
+                   sdesc_sw128(do_a + kk * 2048, C::SUB, 1024), id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars.do_empty[sd]);   // dV is the last reader of dO(i)
+          if (lt + 1 < n) issue_s(gi + 1);
+          if (!(ok = wait1(bars.ds_full, gi & 1, wc, ERR_WAIT_MMA))) break;
+          tc_fence_after();
+          if constexpr (DET) {
+            // dK += dS^T Q with dS^T packed in TMEM like P^T (in the dP^T columns)
 #pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ss(t_dk, sdesc_sw128(ds_a + (kk / 4) * C::SUB + (kk % 4) * 32, 16, 1024),
-                   sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.q_empty[s]);
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_ts(t_dk, t_dp + (kk / 4) * 64 + (kk % 4) * 8,
+                     sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc,
+                     (lt > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bars.q_empty[s]);
+          } else {
+            // dQ = dS K, then dK += dS^T Q (A = dS^T: K-major view of the dS
+            // boxes): dQ first, so that its read-out (which gates the next
+            // dP) starts a product earlier
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_ss(t_dp, sdesc_sw128(ds_a + kk * 2048, C::SUB, 1024),
+                     sdesc_sw128(k_a + kk * 2048, C::SUB, 1024), id_dq, kk > 0 ? 1u : 0u);
+            mma_commit(bars.dq_full);
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_ss(t_dk, sdesc_sw128(ds_a + (kk / 4) * C::SUB + (kk % 4) * 32, 16, 1024),
+                     sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc,
+                     (lt > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bars.q_empty[s]);
+          }
         }
+        // every MMA of this item: its K/V buffers are free, dK and dV final
+        mma_commit(bars.kv_empty);
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      g += n;
+      ++kph;
+    }
+    if (lane == 0 && issued) {
       mma_commit(bars.drain);
       wait1(bars.drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
     }
@@ -406,14 +529,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // of S^T / P^T / dP^T / dS^T, and columns [h*D/2, (h+1)*D/2) of dQ, dK, dV.
     const int h = warp / 4;
     const int r = (warp % 4) * 32 + lane;            // key within the tile = TMEM lane
-    const int key = key0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const float sl2 = p.scale * kLog2e;
     float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);
     uint8_t* ds_s = smem + C::OFF_DS;
     constexpr int HD = D / 2;      // dQ / dK / dV columns per warpgroup
+    // the current item: its ring slot (read from shared memory where needed,
+    // to keep the tile loop's registers few) and first global step
+    volatile BwdSlot* cur = slots;
+    float kb = -INFINITY;          // this thread's key: bias (log2 domain), -inf past the end
 
-    // dQ of query tile `it` (TMEM lane = query row): this warpgroup's columns
+    // dQ of global step gi (TMEM lane = query row): this warpgroup's columns
     // are read out of TMEM at once (the columns go back to the MMA warp)
     // and reduce-added into the fp32 accumulator with TMA in boxes
     // of 32 rows x 32 columns (4 KiB, 128-byte swizzled) staged in this
@@ -441,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         bulk_commit_group();
       }
     };
-    auto dq_readout = [&](int it) -> bool {
-      if (!wait_warp(bars.dq_full, it & 1, wc, ERR_WAIT_EPILOGUE)) return false;
+    auto dq_readout = [&](int gi) -> bool {
+      if (!wait_warp(bars.dq_full, gi & 1, wc, ERR_WAIT_EPILOGUE)) return false;
       tc_fence_after();
       uint32_t x[32];
       tmem_ld32(lane_base + 128 + h * HD, x);
@@ -450,8 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive_warp(bars.dq_empty);
-      hold_row0 = sv.q_off + q_row0(it) + (warp % 4) * 32;
-      hold_qc = q_coord(q_head(it));
+      const int lt = gi - cur->g0, nqh = cur->nqh;
+      hold_row0 = cur->q_off + (cur->i0 + lt % nqh) * kT + (warp % 4) * 32;
+      hold_qc = cur->qc0 + lt / nqh;
       stage_box(x, h * HD, hold_row0, hold_qc);
       return true;
     };
@@ -459,18 +586,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     auto dq_finish = [&]() {
       if constexpr (HD > 32) stage_box(dq_hold, h * HD + 32, hold_row0, hold_qc);
     };
-    // P^T of query tile `it` = exp2(S^T * scale*log2e + bias - LSE2), masked
+    // P^T of global step gi = exp2(S^T * scale*log2e + bias - LSE2), masked
     // -> 0, kept in fp32 registers for dS; packed bf16 copy to TMEM for dV.
     float P[64];
-    auto compute_p = [&](int it) -> bool {
-      const int q0 = q_row0(it);
+    auto compute_p = [&](int gi) -> bool {
+      const int q0 = (cur->i0 + (gi - cur->g0) % cur->nqh) * kT;
+      const int off = cur->off, key = cur->key0 + r;
       // this tile's base-2 LSE (staged by TMA with Q) for this warpgroup's columns
-      if (!wait_warp(&bars.q_full[it & 1], (it >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) return false;
-      const float* stl = stat + (it & 1) * 2 * kT + h * 64;
-      if (!wait_warp(bars.s_full, it & 1, wc, ERR_WAIT_SOFTMAX)) return false;
+      if (!wait_warp(&bars.q_full[gi & 1], (gi >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) return false;
+      const float* stl = stat + (gi & 1) * 2 * kT + h * 64;
+      if (!wait_warp(bars.s_full, gi & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
-      const bool need_mask = CAUSAL && ((long)q0 + off < (long)key0 + kT - 1);
-      const long thr = (long)key - off - q0 - h * 64;   // local column < thr -> masked
+      const bool need_mask = CAUSAL && (q0 + off < key - r + kT - 1);
+      const int thr = key - off - q0 - h * 64;   // local column < thr -> masked
       uint32_t* sv = reinterpret_cast<uint32_t*>(P);
       tmem_ld32(lane_base + h * 64, sv);
       tmem_ld32(lane_base + h * 64 + 32, sv + 32);
@@ -504,12 +632,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       mbar_arrive_warp(bars.p_full);
       return true;
     };
-    // dS^T = scale * P^T o (dP^T - D) of query tile `it`, into the dS boxes
+    // dS^T = scale * P^T o (dP^T - D) of global step gi, into the dS boxes
     // in shared memory (A operand of dK += dS^T Q and of dQ = dS K).
-    auto compute_ds = [&](int it) -> bool {
-      const float* std_ = stat + (it & 1) * 2 * kT + kT + h * 64;   // -scale * D
+    auto compute_ds = [&](int gi) -> bool {
+      const float* std_ = stat + (gi & 1) * 2 * kT + kT + h * 64;   // -scale * D
       const uint64_t sc2 = f2_pack(p.scale, p.scale);
-      if (!wait_warp(bars.dp_full, it & 1, wc, ERR_WAIT_SOFTMAX)) return false;
+      if (!wait_warp(bars.dp_full, gi & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
       // two chunks of 32 query columns, to keep the live registers low
 #pragma unroll
@@ -560,76 +688,102 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       return true;
     };
 
-    // Order per tile i: dS(i), the second dQ box of tile i-1, P(i+1) (its
-    // S^T was issued right after dV(i)), then the read-out of dQ(i); P(0)
-    // first.
-    int it = 0;
-    bool ok = n == 0 || compute_p(0);
-    for (; ok && it < n; ++it) {
-      if (!(ok = compute_ds(it))) break;
-      if (!DET && it > 0) dq_finish();
-      if (it + 1 < n && !(ok = compute_p(it + 1))) break;
-      if (!DET && !(ok = dq_readout(it))) break;   // the last one: every MMA of this CTA is done
-    }
-    if (!DET) {
-      if (ok && it == n && n > 0) {
-        dq_finish();
-        // dK of the last tile is issued after its dQ: wait for every MMA of
-        // the CTA (the MMA warp's final commit) before reading dK and dV
-        ok = wait_warp(bars.drain, 0, wc, ERR_WAIT_EPILOGUE);
-        tc_fence_after();
+    // The staging of dK and dV: the Q stages in the deterministic form (one
+    // item per CTA: free once its MMAs are done); otherwise the dQ staging
+    // and dS buffers (64 KiB together), whose next writers wait until TMA
+    // has read the staging, so the next item's loads are not held up.
+    uint8_t* stage = DET ? smem + C::OFF_Q : smem + C::OFF_DQST;   // [dV, dK][D/64 boxes][128 keys][128 B]
+    // barrier of the eight compute warps, on an mbarrier so that a warp that
+    // has stopped makes the others' wait run out instead of hang. Use j of
+    // item u (j = 0..2, the first only for u > 0) is its phase 3u - 1 + j.
+    auto cw_sync = [&](int u, int j) -> bool {
+      mbar_arrive_warp(bars.cw);
+      return wait_warp(bars.cw, (3 * u - 1 + j) & 1, wc, ERR_WAIT_EPILOGUE);
+    };
+    for (int u = 0;; ++u) {
+      if (!wait_warp(&bars.sched_full[u & 1], (u >> 1) & 1, wc, ERR_WAIT_LOAD)) break;
+      cur = slots + (u & 1);   // held until this item's epilogue is done with it
+      if (cur->w < 0) break;
+      const int n = cur->n;
+      {
+        const int key = cur->key0 + r;
+        kb = key < cur->nk ? (BIAS ? a.bias[(size_t)cur->bias_row + key] * kLog2e : 0.f) : -INFINITY;
       }
-      if (lane == 0) bulk_wait_group0();   // reductions complete before the CTA exits
-      __syncwarp();
-    } else if (ok && it == n && n > 0) {
-      // dq_full follows the last dK here
-      ok = wait_warp(bars.dq_full, 0, wc, ERR_WAIT_EPILOGUE);
-      tc_fence_after();
-    }
-    // ---- dK, dV of this key tile. Each thread reads its key row (this
-    // warpgroup's half of the columns) out of TMEM and stages it in shared
-    // memory (the Q stages, free once every MMA is done) as the 128-byte-
-    // swizzled 64-column boxes TMA uses; one thread then stores the tiles
-    // with TMA, and the CTA waits only until TMA has read them, so the
-    // global writes drain while the next CTA starts. A packed sequence's
-    // ragged last tile is written with plain coalesced stores instead (a
-    // 128-row box would run into the next sequence's rows).
-    const bool do_epi = ok && it == n;
-    uint8_t* stage = smem + C::OFF_Q;   // [dV, dK][D/64 boxes][128 keys][128 B]
-    if (do_epi) {
-      const bool have = n > 0;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {   // 0: dV, 1: dK
-#pragma unroll
-        for (int c0 = 0; c0 < HD; c0 += 32) {
-          uint32_t x[32];
-          if (have) {
-            tmem_ld32(lane_base + 256 + which * D + h * HD + c0, x);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = 0u;
-          }
-          uint32_t pkd[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
-          const int col = h * HD + c0;   // first column of these 32
-          uint8_t* rowp = stage + which * C::TILE + (col / 64) * C::SUB + r * 128;
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const int j = (col % 64) / 8 + v4;
-            *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) * 16)) =
-                make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
-          }
+
+      // Order per tile i: dS(i), the second dQ box of tile i-1, P(i+1) (its
+      // S^T was issued right after dV(i)), then the read-out of dQ(i); P of
+      // the item's first tile first.
+      bool ok = true;
+      int lt = 0;
+      const int g = cur->g0;
+      if (n > 0) ok = compute_p(g);
+      if (u > 0) {
+        // every compute warp passes here once per item, even after a failed
+        // wait: the previous item's dK/dV staging (the dS and dQ staging
+        // buffers) has been read by TMA before anything writes them again
+        if (!DET && threadIdx.x == 0) bulk_wait_group_read0();
+        if (!cw_sync(u, 0)) ok = false;
+      }
+      if (n > 0) {
+        for (; ok && lt < n; ++lt) {
+          const int gi = g + lt;
+          if (!(ok = compute_ds(gi))) break;
+          if (!DET && lt > 0) dq_finish();
+          if (lt + 1 < n && !(ok = compute_p(gi + 1))) break;
+          if (!DET && !(ok = dq_readout(gi))) break;
+        }
+        if (ok) {
+          if (!DET) dq_finish();
+          // every MMA of the item is done (the last dK follows the last dQ)
+          ok = wait_warp(bars.kv_empty, cur->kph & 1, wc, ERR_WAIT_EPILOGUE);
+          tc_fence_after();
         }
       }
-      fence_proxy_async_smem();   // the generic-proxy writes, before TMA reads them
-    }
-    // every compute thread arrives here; the tiles are written only if every
-    // warp staged its part
-    if (named_bar_and(1, 2 * kT, do_epi)) {
-      const bool ragged = p.cu_k != nullptr && key0 + kT > Nk;
+      // ---- dK, dV of this key tile. Each thread reads its key row (this
+      // warpgroup's half of the columns) out of TMEM and stages it in shared
+      // memory as the 128-byte-swizzled 64-column boxes TMA uses; one thread
+      // then stores the tiles with TMA. A packed sequence's ragged last tile
+      // is written with plain coalesced stores instead (a 128-row box would
+      // run into the next sequence's rows). Every compute warp reaches both
+      // barriers once per item.
+      if (!DET && lane == 0) bulk_wait_group_read0();   // this warp's dQ boxes have been read
+      if (!cw_sync(u, 1)) ok = false;                    // ... and every other warp's
+      const bool do_epi = ok;
+      if (do_epi) {
+        const bool have = n > 0;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {   // 0: dV, 1: dK
+#pragma unroll
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            uint32_t x[32];
+            if (have) {
+              tmem_ld32(lane_base + 256 + which * D + h * HD + c0, x);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) x[e] = 0u;
+            }
+            uint32_t pkd[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+            const int col = h * HD + c0;   // first column of these 32
+            uint8_t* rowp = stage + which * C::TILE + (col / 64) * C::SUB + r * 128;
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const int j = (col % 64) / 8 + v4;
+              *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) * 16)) =
+                  make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+            }
+          }
+        }
+        fence_proxy_async_smem();   // the generic-proxy writes, before TMA reads them
+      }
+      // the tiles are written only if every warp staged its part (a warp
+      // whose wait failed has raised the abort flag before arriving)
+      if (!cw_sync(u, 2) || !do_epi || *abort_flag) break;
+      const BwdItem t = bwd_item<CAUSAL>(a, cur->w);
+      const bool ragged = p.cu_k != nullptr && t.key0 + kT > t.Nk;
       if (!ragged) {
         if (threadIdx.x == 0) {
 #pragma unroll
@@ -637,25 +791,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
               tma_store_3d(which ? &a.tm_dk : &a.tm_dv, stage + which * C::TILE + c * C::SUB,
-                           c * 64, sv.k_off + key0, sv.hk);
+                           c * 64, t.sv.k_off + t.key0, t.sv.hk);
           bulk_commit_group();
-          bulk_wait_group_read0();   // shared memory may be released
         }
       } else {
         constexpr int CPR = D / 8;   // 16-byte pieces per row
         for (int idx = threadIdx.x; idx < 2 * kT * CPR; idx += 2 * kT) {
           const int which = idx / (kT * CPR), rem = idx % (kT * CPR);
           const int row = rem / CPR, c = rem % CPR;
-          if (key0 + row < Nk) {
+          if (t.key0 + row < t.Nk) {
             const uint4 v = *reinterpret_cast<const uint4*>(
                 stage + which * C::TILE + (c / 8) * C::SUB + row * 128 + (((c % 8) ^ (row & 7)) * 16));
             uint16_t* dst = (which ? a.dk : a.dv) +
-                            ((size_t)sv.hk * sv.krows + sv.k_off + key0 + row) * D + c * 8;
+                            ((size_t)t.sv.hk * t.sv.krows + t.sv.k_off + t.key0 + row) * D + c * 8;
             *reinterpret_cast<uint4*>(dst) = v;
           }
         }
       }
+      mbar_arrive_warp(&bars.sched_empty[u & 1]);   // done with the slot
     }
+    // reductions and stores complete before the CTA exits
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -674,13 +831,19 @@ cudaError_t launch_main(const BwdBf16Args& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
   if (e != cudaSuccess) return e;
   const long BHkv = (long)a.p.B * a.p.Hkv;
-  const long n_kt = (a.p.Nk + kT - 1) / kT;
-  // heads per ordering group: the Q and dO every CTA of a key/value head
+  const long n_items = BHkv * ((a.p.Nk + kT - 1) / kT);
+  // heads per ordering group: the Q and dO every item of a key/value head
   // streams (all query heads of its group) within ~48 MiB of L2
   const long q_bytes = 2L * (a.p.H / a.p.Hkv) * a.p.Nq * D * 2;
   BwdBf16Args b = a;
   b.head_group = (int)std::max(1L, std::min(BHkv, (48L << 20) / std::max(q_bytes, 1L)));
-  kern<<<(unsigned)(BHkv * n_kt), kThreads, C::BYTES, s>>>(b);
+  long grid = n_items;
+  if (!DET) {
+    // persistent: one CTA per SM, items from the counter
+    grid = std::min(n_items, (long)std::max(a.num_sms, 1));
+    if ((e = cudaMemsetAsync(a.sched, 0, sizeof(int), s)) != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)grid, kThreads, C::BYTES, s>>>(b);
   return cudaGetLastError();
 }
 

@@ -143,10 +143,11 @@ Fp8Ws fp8_ws_layout(int B, int H, int Hkv, int Nq, int Nk, int d) {
 }
 
 // Workspace of the backward: padded statistics for B*H (sequence, head)
-// pairs of nq_max rows, then the fp32 dQ accumulator of `dq_rows` rows.
+// pairs of nq_max rows, then the fp32 dQ accumulator of `dq_rows` rows and,
+// with it, the main kernel's work-item counter.
 size_t bwd_ws_bytes(int B, int H, int nq_max, size_t dq_rows, int d) {
   const size_t prow = (size_t)B * H * (((size_t)nq_max + 127) / 128 * 128);
-  return 2 * round256(prow * 4) + round256(dq_rows * (size_t)d * 4);
+  return 2 * round256(prow * 4) + (dq_rows ? round256(dq_rows * (size_t)d * 4) + 256 : 0);
 }
 
 
@@ -389,6 +390,9 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   a.D = reinterpret_cast<float*>(ws);
   a.lse2 = reinterpret_cast<float*>(ws + round256(prow * 4));
   a.dq_acc = det ? nullptr : reinterpret_cast<float*>(ws + 2 * round256(prow * 4));
+  a.sched = det ? nullptr
+                : reinterpret_cast<int*>(ws + 2 * round256(prow * 4) +
+                                         round256(dq_rows * (size_t)d * 4));
   if (!det && (stages & fa::BWD_MAIN) &&
       (st = make_map_f32_acc(&a.tm_dqacc, a.dq_acc, qh, qn, d)) != FA_OK)
     return st;

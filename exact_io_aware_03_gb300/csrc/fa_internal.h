@@ -103,6 +103,8 @@ struct BwdBf16Args {
   float* lse2;         // workspace: -LSE * log2(e), [B*H][nq_pad] (-inf for fully
                        // masked rows and in the padding)
   float* dq_acc;       // workspace: fp32 dQ accumulator [B][H][Nq][d]
+  int* sched;          // workspace: work-item counter of the persistent main kernel
+                       // (zeroed by the launcher before each launch)
   uint16_t* dq;
   uint16_t* dk;
   uint16_t* dv;

@@ -159,7 +159,8 @@ fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, const floa
 /*
  * Bytes of device workspace fa_bwd needs: -scale * D with D = rowsum(dO o O),
  * and -LSE rescaled to base 2, each fp32 [B*H][Nq rounded up to a multiple of 128],
- * and an fp32 dQ accumulator [B,H,Nq,d], each starting on a 256-byte boundary.
+ * an fp32 dQ accumulator [B,H,Nq,d] and a 256-byte work-item counter of the main
+ * launch (reset by it), each starting on a 256-byte boundary.
  * Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d);

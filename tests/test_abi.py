@@ -53,11 +53,14 @@ def test_workspace_size(lib):
     B, H, Nq, Nk, d = 4, 16, 4096, 4096, 128
     rows = B * H * Nq
     r256 = lambda x: (x + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_size(B, H, Nq, Nk, d) == 2 * r256(rows * 4) + r256(rows * d * 4)
+    # statistics, the fp32 dQ accumulator and 256 bytes for the main kernel's
+    # work-item counter
+    assert fa.fa_bwd_workspace_size(B, H, Nq, Nk, d) == 2 * r256(rows * 4) + r256(rows * d * 4) + 256
     assert fa.fa_bwd_workspace_size(0, 1, 1, 1, 64) == 0
     # per-row statistics are padded to 128 rows per head
-    assert fa.fa_bwd_workspace_size(1, 1, 3, 1, 64) == 2 * 512 + 768
-    assert fa.fa_bwd_workspace_size(2, 3, 129, 5, 128) == 2 * r256(6 * 256 * 4) + r256(6 * 129 * 512)
+    assert fa.fa_bwd_workspace_size(1, 1, 3, 1, 64) == 2 * 512 + 768 + 256
+    assert fa.fa_bwd_workspace_size(2, 3, 129, 5, 128) == (2 * r256(6 * 256 * 4) + r256(6 * 129 * 512)
+                                                           + 256)
 
 
 FAKE = 1 << 20          # 16-byte aligned, never dereferenced: rejected before any launch

@@ -537,7 +537,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // the current item: its ring slot (read from shared memory where needed,
     // to keep the tile loop's registers few) and first global step
     volatile BwdSlot* cur = slots;
-    float kb = -INFINITY;          // this thread's key: bias (log2 domain), -inf past the end
 
     // dQ of global step gi (TMEM lane = query row): this warpgroup's columns
     // are read out of TMEM at once (the columns go back to the MMA warp)
@@ -550,7 +549,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // buffer is never used for staging.
     uint8_t* dq_stage = smem + C::OFF_DQST + warp * 4096;
     uint32_t dq_hold[32];   // second box of the pending dQ (d = 128)
-    int hold_row0 = 0, hold_qc = 0;
     auto stage_box = [&](const uint32_t* v32, int col, int row0, int qc) {
       if (lane == 0) bulk_wait_group_read0();   // the previous box has been read
       __syncwarp();
@@ -577,14 +575,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tc_fence_before();
       mbar_arrive_warp(bars.dq_empty);
       const int lt = gi - cur->g0, nqh = cur->nqh;
-      hold_row0 = cur->q_off + (cur->i0 + lt % nqh) * kT + (warp % 4) * 32;
-      hold_qc = cur->qc0 + lt / nqh;
-      stage_box(x, h * HD, hold_row0, hold_qc);
+      stage_box(x, h * HD, cur->q_off + (cur->i0 + lt % nqh) * kT + (warp % 4) * 32,
+                cur->qc0 + lt / nqh);
       return true;
     };
-    // the second box of the pending dQ (no-op at d = 64, which has one)
-    auto dq_finish = [&]() {
-      if constexpr (HD > 32) stage_box(dq_hold, h * HD + 32, hold_row0, hold_qc);
+    // the second box of the pending dQ of global step gi (no-op at d = 64,
+    // which has one)
+    auto dq_finish = [&](int gi) {
+      if constexpr (HD > 32) {
+        const int lt = gi - cur->g0, nqh = cur->nqh;
+        stage_box(dq_hold, h * HD + 32, cur->q_off + (cur->i0 + lt % nqh) * kT + (warp % 4) * 32,
+                  cur->qc0 + lt / nqh);
+      }
     };
     // P^T of global step gi = exp2(S^T * scale*log2e + bias - LSE2), masked
     // -> 0, kept in fp32 registers for dS; packed bf16 copy to TMEM for dV.
@@ -598,6 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       if (!wait_warp(bars.s_full, gi & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
       const bool need_mask = CAUSAL && (q0 + off < key - r + kT - 1);
+      // the key's term: its bias (log2 domain), -inf past the end of a ragged tile
+      const float kb =
+          key < cur->nk ? (BIAS ? a.bias[(size_t)cur->bias_row + key] * kLog2e : 0.f) : -INFINITY;
       const int thr = key - off - q0 - h * 64;   // local column < thr -> masked
       uint32_t* sv = reinterpret_cast<uint32_t*>(P);
       tmem_ld32(lane_base + h * 64, sv);
@@ -705,10 +710,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       cur = slots + (u & 1);   // held until this item's epilogue is done with it
       if (cur->w < 0) break;
       const int n = cur->n;
-      {
-        const int key = cur->key0 + r;
-        kb = key < cur->nk ? (BIAS ? a.bias[(size_t)cur->bias_row + key] * kLog2e : 0.f) : -INFINITY;
-      }
 
       // Order per tile i: dS(i), the second dQ box of tile i-1, P(i+1) (its
       // S^T was issued right after dV(i)), then the read-out of dQ(i); P of
@@ -728,12 +729,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         for (; ok && lt < n; ++lt) {
           const int gi = g + lt;
           if (!(ok = compute_ds(gi))) break;
-          if (!DET && lt > 0) dq_finish();
+          if (!DET && lt > 0) dq_finish(gi - 1);
           if (lt + 1 < n && !(ok = compute_p(gi + 1))) break;
           if (!DET && !(ok = dq_readout(gi))) break;
         }
         if (ok) {
-          if (!DET) dq_finish();
+          if (!DET) dq_finish(g + n - 1);
           // every MMA of the item is done (the last dK follows the last dQ)
           ok = wait_warp(bars.kv_empty, cur->kph & 1, wc, ERR_WAIT_EPILOGUE);
           tc_fence_after();

@@ -71,44 +71,59 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
   // (added to the base-2 score). Padding rows and rows that see no key get 0
   // and -inf: their recomputed P is exactly 0.
   constexpr int LPR = D / 8;          // lanes per row, 8 bf16 (16 B) per lane
-  constexpr int RPW = 32 / LPR;       // rows per warp step
+  constexpr int RPW = 32 / LPR;       // rows per warp and unrolled step
+  constexpr int U = 4;                // unrolled steps: U rows' loads in flight per lane
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, li = lane % LPR;
   const long warp_g = ((long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const long nwarps = ((long)gridDim.x * blockDim.x) / 32;
   const long prows = (long)p.B * p.H * nq_pad;
-  for (long r0 = warp_g * RPW; r0 < prows; r0 += nwarps * RPW) {
-    const long pr = r0 + sub;            // padded statistics row
-    const bool in = pr < prows;
-    const int bh = (int)(min(pr, prows - 1) / nq_pad);
-    const int i = (int)(pr - (long)bh * nq_pad);
-    const SeqView sv = seq_view(p, bh / p.H, bh % p.H);
-    if (in && i == 0 && sv.bad) atomicOr(err, ERR_BAD_SEQLEN);
-    const bool valid = in && i < sv.len_q;
-    const long row = (long)sv.hq * sv.qrows + sv.q_off + i;   // row of O, dO, LSE, dQ accumulator
-    float acc = 0.f;
-    if (valid) {
-      const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[li];
-      const uint4 g = reinterpret_cast<const uint4*>(dO + row * D)[li];
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+  for (long r0 = warp_g * RPW * U; r0 < prows; r0 += nwarps * RPW * U) {
+    uint4 av[U], gv[U];
+    float L[U];
+    long row[U];
+    bool valid[U];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(gv[e] << 16), acc);
-        acc = fmaf(__uint_as_float(av[e] & 0xffff0000u), __uint_as_float(gv[e] & 0xffff0000u),
-                   acc);
-      }
-      if (dq_acc) {
-        float4* z = reinterpret_cast<float4*>(dq_acc + row * D);
-        z[2 * li] = make_float4(0.f, 0.f, 0.f, 0.f);
-        z[2 * li + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < U; ++u) {
+      const long pr = r0 + u * RPW + sub;   // padded statistics row
+      const bool in = pr < prows;
+      const int bh = (int)(min(pr, prows - 1) / nq_pad);
+      const int i = (int)(pr - (long)bh * nq_pad);
+      const SeqView sv = seq_view(p, bh / p.H, bh % p.H);
+      if (in && i == 0 && sv.bad) atomicOr(err, ERR_BAD_SEQLEN);
+      valid[u] = in && i < sv.len_q;
+      row[u] = (long)sv.hq * sv.qrows + sv.q_off + i;   // row of O, dO, LSE, dQ accumulator
+      av[u] = gv[u] = make_uint4(0u, 0u, 0u, 0u);
+      L[u] = -INFINITY;
+      if (valid[u]) {
+        av[u] = reinterpret_cast<const uint4*>(o + row[u] * D)[li];
+        gv[u] = reinterpret_cast<const uint4*>(dO + row[u] * D)[li];
+        if (li == 0) L[u] = lse[row[u]];
       }
     }
 #pragma unroll
-    for (int w = LPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-    if (in && li == 0) {
-      Dv[pr] = valid ? -p.scale * acc : 0.f;
-      const float L = valid ? lse[row] : -INFINITY;
-      lse2[pr] = (L == -INFINITY) ? -INFINITY : -L * kLog2e;
+    for (int u = 0; u < U; ++u) {
+      const long pr = r0 + u * RPW + sub;
+      const uint32_t a4[4] = {av[u].x, av[u].y, av[u].z, av[u].w};
+      const uint32_t g4[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(a4[e] << 16), __uint_as_float(g4[e] << 16), acc);
+        acc = fmaf(__uint_as_float(a4[e] & 0xffff0000u), __uint_as_float(g4[e] & 0xffff0000u),
+                   acc);
+      }
+      if (valid[u] && dq_acc) {
+        float4* z = reinterpret_cast<float4*>(dq_acc + row[u] * D);
+        z[2 * li] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[2 * li + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int w = LPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+      if (pr < prows && li == 0) {
+        Dv[pr] = valid[u] ? -p.scale * acc : 0.f;
+        lse2[pr] = (L[u] == -INFINITY) ? -INFINITY : -L[u] * kLog2e;
+      }
     }
   }
 }
@@ -116,10 +131,23 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 // ------------------------------------------------------------------ post
 __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ acc,
                                                        uint16_t* __restrict__ dq, long n4) {
-  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-       i += (long)gridDim.x * blockDim.x) {
-    const float4 v = reinterpret_cast<const float4*>(acc)[i];
-    reinterpret_cast<uint2*>(dq)[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  // four float4 loads in flight per thread
+  constexpr int U = 4;
+  const long stride = (long)gridDim.x * blockDim.x;
+  for (long i0 = (long)blockIdx.x * blockDim.x + threadIdx.x; i0 < n4; i0 += stride * U) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long i = i0 + u * stride;
+      if (i < n4) v[u] = reinterpret_cast<const float4*>(acc)[i];
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long i = i0 + u * stride;
+      if (i < n4)
+        reinterpret_cast<uint2*>(dq)[i] =
+            make_uint2(pack_bf16x2(v[u].x, v[u].y), pack_bf16x2(v[u].z, v[u].w));
+    }
   }
 }
 

@@ -444,16 +444,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);    // S^T, dP^T
     constexpr uint32_t id_acc = idesc_bf16_f32(kT, D, false, true);    // dV, dK (A K-major)
     constexpr uint32_t id_dq = idesc_bf16_f32(kT, D, true, true);      // dQ (A = dS, MN-major)
-    const uint32_t k_a = smem_u32(smem + C::OFF_K), v_a = smem_u32(smem + C::OFF_V);
-    const uint32_t ds_a = smem_u32(smem + C::OFF_DS);
     const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
+    // operand descriptors, built once for the start of shared memory: an
+    // operand's is this plus its byte offset (K-major boxes read along K:
+    // LBO 16; along the 128-row direction: LBO = one box)
+    const uint32_t sbase = smem_u32(smem);
+    const uint64_t dk16 = sdesc_sw128(sbase, 16, 1024), dsub = sdesc_sw128(sbase, C::SUB, 1024);
     // S^T = K Q^T for global step gi (both K-major, 128-byte rows per box)
     auto issue_s = [&](int gi) {
-      const uint32_t q_a = smem_u32(smem + C::OFF_Q + (gi & 1) * C::TILE);
+      const uint32_t q_o = C::OFF_Q + (gi & 1) * C::TILE;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
-        mma_ss(t_s, sdesc_sw128(k_a + o, 16, 1024), sdesc_sw128(q_a + o, 16, 1024), id_s, kk > 0);
+        mma_ss(t_s, sdesc_offset(dk16, C::OFF_K + o), sdesc_offset(dk16, q_o + o), id_s, kk > 0);
       }
       mma_commit(bars.s_full);
     };
@@ -482,8 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         }
         for (int lt = 0; lt < n && ok; ++lt) {
           const int gi = g + lt, s = gi & 1, sd = gi % C::ND;
-          const uint32_t q_a = smem_u32(smem + C::OFF_Q + s * C::TILE);
-          const uint32_t do_a = smem_u32(smem + C::OFF_DO + sd * C::TILE);
+          const uint32_t q_o = C::OFF_Q + s * C::TILE, do_o = C::OFF_DO + sd * C::TILE;
           // dP^T = V dO^T, once dQ of the previous tile has left TMEM (DET: the
           // dS^T of the previous tile in these columns was read by dK, an
           // earlier MMA)
@@ -493,8 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
-            mma_ss(t_dp, sdesc_sw128(v_a + o, 16, 1024), sdesc_sw128(do_a + o, 16, 1024), id_s,
-                   kk > 0);
+            mma_ss(t_dp, sdesc_offset(dk16, C::OFF_V + o), sdesc_offset(dk16, do_o + o), id_s, kk > 0);
           }
           mma_commit(bars.dp_full);
           // dV(i) and S(i+1) are issued back to back once both can go: a wait
@@ -508,8 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           // [0,32), [64,128) in [64,96))
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8,
-                   sdesc_sw128(do_a + kk * 2048, C::SUB, 1024), id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8, sdesc_offset(dsub, do_o + kk * 2048), id_acc,
+                   (lt > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars.do_empty[sd]);   // dV is the last reader of dO(i)
           if (lt + 1 < n) issue_s(gi + 1);
           if (!(ok = wait1(bars.ds_full, gi & 1, wc, ERR_WAIT_MMA))) break;
@@ -518,9 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             // dK += dS^T Q with dS^T packed in TMEM like P^T (in the dP^T columns)
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
-              mma_ts(t_dk, t_dp + (kk / 4) * 64 + (kk % 4) * 8,
-                     sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc,
-                     (lt > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(t_dk, t_dp + (kk / 4) * 64 + (kk % 4) * 8, sdesc_offset(dsub, q_o + kk * 2048),
+                     id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&bars.q_empty[s]);
           } else {
             // dQ = dS K, then dK += dS^T Q (A = dS^T: K-major view of the dS
@@ -528,14 +528,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             // dP) starts a product earlier
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
-              mma_ss(t_dp, sdesc_sw128(ds_a + kk * 2048, C::SUB, 1024),
-                     sdesc_sw128(k_a + kk * 2048, C::SUB, 1024), id_dq, kk > 0 ? 1u : 0u);
+              mma_ss(t_dp, sdesc_offset(dsub, C::OFF_DS + kk * 2048),
+                     sdesc_offset(dsub, C::OFF_K + kk * 2048), id_dq, kk > 0 ? 1u : 0u);
             mma_commit(bars.dq_full);
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
-              mma_ss(t_dk, sdesc_sw128(ds_a + (kk / 4) * C::SUB + (kk % 4) * 32, 16, 1024),
-                     sdesc_sw128(q_a + kk * 2048, C::SUB, 1024), id_acc,
-                     (lt > 0 || kk > 0) ? 1u : 0u);
+              mma_ss(t_dk, sdesc_offset(dk16, C::OFF_DS + (kk / 4) * C::SUB + (kk % 4) * 32),
+                     sdesc_offset(dsub, q_o + kk * 2048), id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&bars.q_empty[s]);
           }
         }

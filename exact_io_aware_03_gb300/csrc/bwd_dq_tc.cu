@@ -227,22 +227,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     if (lane == 0 && n > 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);   // S, dP (K-major)
       constexpr uint32_t id_dq = idesc_bf16_f32(kT, D, false, true);    // dQ: B = K, MN-major
-      const uint32_t k_a = smem_u32(smem + C::OFF_K), v_a = smem_u32(smem + C::OFF_V);
       const uint32_t t_s = tmem, t_dp = tmem + 128, t_dq = tmem + 256;
       const uint32_t t_q = tmem + 256 + D, t_do = tmem + 256 + D + D / 2;
+      // operand descriptors, built once for the start of shared memory: an
+      // operand's is this plus its byte offset
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t dk16 = sdesc_sw128(sbase, 16, 1024), dsub = sdesc_sw128(sbase, C::SUB, 1024);
       // D = A B^T over the head dimension: A (Q or dO) in TMEM, B (K or V) a
-      // K-major tile of 64-column boxes
-      auto issue_nt = [&](uint32_t d, uint32_t a_t, uint32_t b_s) {
+      // K-major tile of 64-column boxes at byte offset b_o
+      auto issue_nt = [&](uint32_t d, uint32_t a_t, uint32_t b_o) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
-          mma_ts(d, a_t + kk * 8, sdesc_sw128(b_s + o, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          mma_ts(d, a_t + kk * 8, sdesc_offset(dk16, b_o + o), id_s, kk > 0 ? 1u : 0u);
         }
       };
       bool ok = wait1(qt_ready, 0, wc, ERR_WAIT_MMA) && wait1(&k_full[0], 0, wc, ERR_WAIT_MMA);
       if (ok) {
         tc_fence_after();
-        issue_nt(t_s, t_q, k_a);
+        issue_nt(t_s, t_q, C::OFF_K);
         mma_commit(s_full);
       }
       // Every wait of an iteration but the one for dS(i) comes first, while
@@ -259,11 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         tc_fence_after();
         // dP = dO V^T (the dP columns are free: dQ(i-1), which read dS(i-1)
         // there, was issued before and MMAs complete in order)
-        issue_nt(t_dp, t_do, v_a + sv_ * C::TILE);
+        issue_nt(t_dp, t_do, C::OFF_V + sv_ * C::TILE);
         mma_commit(dp_full);
         mma_commit(&v_empty[sv_]);
         if (next) {
-          issue_nt(t_s, t_q, k_a + s1 * C::TILE);
+          issue_nt(t_s, t_q, C::OFF_K + s1 * C::TILE);
           mma_commit(s_full);
         }
         // dQ += dS K_j: dS packed bf16, keys [0,64) in TMEM columns [128,160),
@@ -273,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
           mma_ts(t_dq, t_dp + (kk / 4) * 64 + (kk % 4) * 8,
-                 sdesc_sw128(k_a + s * C::TILE + kk * 2048, C::SUB, 1024), id_dq,
+                 sdesc_offset(dsub, C::OFF_K + s * C::TILE + kk * 2048), id_dq,
                  (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&k_empty[s]);
       }

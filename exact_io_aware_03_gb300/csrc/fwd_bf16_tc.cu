@@ -309,33 +309,36 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
       const uint32_t k_addr = smem_u32(smem + C::OFF_K);
       const uint32_t v_addr = smem_u32(smem + C::OFF_V);
       auto active = [&](int t, int j) { return j >= lo && j < hi_t[t]; };
+      // operand descriptors of each stage, built once; an instruction's
+      // descriptor is the stage's plus its byte offset
+      const uint64_t qd0 = sdesc_sw128(q_addr, 16, 1024);
+      const uint64_t kd0 = sdesc_sw128(k_addr, 16, 1024);
+      const uint64_t vd0 = FP8 ? sdesc_sw128(v_addr, 16, 1024) : sdesc_sw128(v_addr, C::SUB, 1024);
       auto issue_s = [&](int t, int s) {
-        const uint32_t qa = q_addr + t * C::TILE, ka = k_addr + s * C::TILE;
+        const uint64_t qd = sdesc_offset(qd0, t * C::TILE), kd = sdesc_offset(kd0, s * C::TILE);
         // K steps of 32 bytes (16 bf16 or 32 e4m3) along the 128-byte rows
 #pragma unroll
         for (int kk = 0; kk < D * C::EB / 32; ++kk) {
           const uint32_t off = (kk / 4) * C::SUB + (kk % 4) * 32;
           if constexpr (FP8)
-            mma_ss_f8(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024),
-                      sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+            mma_ss_f8(tmem + t * 128, sdesc_offset(qd, off), sdesc_offset(kd, off), idesc_s, kk > 0);
           else
-            mma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024),
-                   sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+            mma_ss(tmem + t * 128, sdesc_offset(qd, off), sdesc_offset(kd, off), idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int s, bool acc) {
-        const uint32_t va = v_addr + s * C::TILE;
+        const uint64_t vd = sdesc_offset(vd0, s * C::TILE);
         if constexpr (FP8) {
           // P as packed e4m3 (4 keys per TMEM column): 32 keys per K step
 #pragma unroll
           for (int kk = 0; kk < kBN / 32; ++kk)
-            mma_ts_f8(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
-                      sdesc_sw128(va + kk * 32, 16, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
+            mma_ts_f8(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_offset(vd, kk * 32), idesc_pv,
+                      (acc || kk > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
-                   sdesc_sw128(va + kk * 2048, C::SUB, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_offset(vd, kk * 2048), idesc_pv,
+                   (acc || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = true;

@@ -323,6 +323,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Descriptor of the operand `off` bytes (a multiple of 16) past the one `d`
+// describes: the start address is bits [0,14) of the descriptor in 16-byte
+// units, and shared-memory addresses stay below 256 KiB, so the field does
+// not carry: one 32-bit add on the low word.
+__device__ __forceinline__ uint64_t sdesc_offset(uint64_t d, uint32_t off) {
+  const uint32_t lo = (uint32_t)d + (off >> 4), hi = (uint32_t)(d >> 32);
+  return ((uint64_t)hi << 32) | lo;
+}
+
 #define FA_R8(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
                  "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
 #define FA_W8(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \

@@ -299,7 +299,8 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
     }
   } else if (warp == 9) {
     // ================================================================ MMA issuer
-    if (lane == 0 && any) {
+    // (the whole warp, converged; one elected lane issues each instruction)
+    if (any) {
       constexpr uint32_t idesc_s =
           FP8 ? idesc_e4m3_f32(kBM, kBN, false, false) : idesc_bf16_f32(kBM, kBN, false, false);
       // PV: B = V (MN-major, d contiguous) or, FP8, V^T (K-major, keys contiguous)
@@ -321,9 +322,9 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
         for (int kk = 0; kk < D * C::EB / 32; ++kk) {
           const uint32_t off = (kk / 4) * C::SUB + (kk % 4) * 32;
           if constexpr (FP8)
-            mma_ss_f8(tmem + t * 128, sdesc_offset(qd, off), sdesc_offset(kd, off), idesc_s, kk > 0);
+            mma_ss_f8_w(tmem + t * 128, sdesc_offset(qd, off), sdesc_offset(kd, off), idesc_s, kk > 0);
           else
-            mma_ss(tmem + t * 128, sdesc_offset(qd, off), sdesc_offset(kd, off), idesc_s, kk > 0);
+            mma_ss_w(tmem + t * 128, sdesc_offset(qd, off), sdesc_offset(kd, off), idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int s, bool acc) {
@@ -332,51 +333,51 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
           // P as packed e4m3 (4 keys per TMEM column): 32 keys per K step
 #pragma unroll
           for (int kk = 0; kk < kBN / 32; ++kk)
-            mma_ts_f8(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_offset(vd, kk * 32), idesc_pv,
+            mma_ts_f8_w(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_offset(vd, kk * 32), idesc_pv,
                       (acc || kk > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_offset(vd, kk * 2048), idesc_pv,
+            mma_ts_w(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_offset(vd, kk * 2048), idesc_pv,
                    (acc || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t)
-        if (hi_t[t] > lo) ok = wait1(&bars.q_full[t], 0, wc, ERR_WAIT_MMA);
-      if (ok) ok = wait1(bars.k0_full, 0, wc, ERR_WAIT_MMA);
+        if (hi_t[t] > lo) ok = wait_warp(&bars.q_full[t], 0, wc, ERR_WAIT_MMA);
+      if (ok) ok = wait_warp(bars.k0_full, 0, wc, ERR_WAIT_MMA);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
           if (active(t, lo)) {
             issue_s(t, 0);
-            mma_commit(&bars.s_full[t]);
+            mma_commit_w(&bars.s_full[t]);
           }
-        mma_commit(bars.k0_empty);
+        mma_commit_w(bars.k0_empty);
       }
       for (int j = lo; j < hi && ok; ++j) {
         const int i = j - lo, s = i % C::NS, s1 = (i + 1) % C::NS;
         // V_i and K_{i+1}
-        if (!wait1(&bars.kv_full[s], (i / C::NS) & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
+        if (!wait_warp(&bars.kv_full[s], (i / C::NS) & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
         tc_fence_after();
         for (int t = 0; t < 2 && ok; ++t) {
           if (active(t, j)) {
-            if (!wait1(&bars.p_full[t], i & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
+            if (!wait_warp(&bars.p_full[t], i & 1, wc, ERR_WAIT_MMA)) { ok = false; break; }
             tc_fence_after();
             issue_pv(t, s, i > 0);
-            mma_commit(&bars.o_done[t]);
+            mma_commit_w(&bars.o_done[t]);
           }
           if (j + 1 < hi && active(t, j + 1)) {
             issue_s(t, s1);
-            mma_commit(&bars.s_full[t]);
+            mma_commit_w(&bars.s_full[t]);
           }
         }
         if (!ok) break;
-        mma_commit(&bars.kv_empty[s]);
+        mma_commit_w(&bars.kv_empty[s]);
       }
       // drain every MMA issued so far before TMEM is released
-      mma_commit(bars.drain);
-      wait1(bars.drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
+      mma_commit_w(bars.drain);
+      wait_warp(bars.drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
     }
   } else {
     // ================================================================ softmax

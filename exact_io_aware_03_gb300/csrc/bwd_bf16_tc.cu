@@ -456,9 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
-        mma_ss(t_s, sdesc_offset(dk16, C::OFF_K + o), sdesc_offset(dk16, q_o + o), id_s, kk > 0);
+        mma_ss_w(t_s, sdesc_offset(dk16, C::OFF_K + o), sdesc_offset(dk16, q_o + o), id_s, kk > 0);
       }
-      mma_commit(bars.s_full);
+      mma_commit_w(bars.s_full);
     };
     int g = 0, kph = 0;
     bool ok = true, issued = false;
@@ -469,15 +469,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(&bars.sched_empty[u & 1]);
       if (w < 0) break;
       if (n == 0) continue;
-      if (lane == 0) {
+      {
+        // (the whole warp, converged; lane 0 issues each instruction)
         // Issue order per query tile i:  dP(i) [after dQ(i-1) left TMEM],
         // dV(i) [after P(i)], S(i+1) [the S columns are free once dV(i) has
         // read P(i)], dQ(i) and dK(i) [after dS(i)]. S(i+1) and the softmax
         // of tile i+1 thus overlap dQ(i) and dK(i). The first dV and dK of
         // an item start from zero: the P/dS warps arrive on P of the item's
         // first tile only after they have read the previous item's dK, dV.
-        ok = !*abort_flag && wait1(bars.kv_full, kph & 1, wc, ERR_WAIT_MMA) &&
-             wait1(&bars.q_full[g & 1], (g >> 1) & 1, wc, ERR_WAIT_MMA);
+        ok = !__any_sync(0xffffffffu, *abort_flag) && wait_warp(bars.kv_full, kph & 1, wc, ERR_WAIT_MMA) &&
+             wait_warp(&bars.q_full[g & 1], (g >> 1) & 1, wc, ERR_WAIT_MMA);
         if (ok) {
           tc_fence_after();
           issue_s(g);
@@ -489,65 +490,64 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           // dP^T = V dO^T, once dQ of the previous tile has left TMEM (DET: the
           // dS^T of the previous tile in these columns was read by dK, an
           // earlier MMA)
-          if (!DET && gi > 0 && !(ok = wait1(bars.dq_empty, (gi - 1) & 1, wc, ERR_WAIT_MMA))) break;
-          if (!(ok = wait1(&bars.do_full[sd], (gi / C::ND) & 1, wc, ERR_WAIT_MMA))) break;
+          if (!DET && gi > 0 && !(ok = wait_warp(bars.dq_empty, (gi - 1) & 1, wc, ERR_WAIT_MMA))) break;
+          if (!(ok = wait_warp(&bars.do_full[sd], (gi / C::ND) & 1, wc, ERR_WAIT_MMA))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
-            mma_ss(t_dp, sdesc_offset(dk16, C::OFF_V + o), sdesc_offset(dk16, do_o + o), id_s, kk > 0);
+            mma_ss_w(t_dp, sdesc_offset(dk16, C::OFF_V + o), sdesc_offset(dk16, do_o + o), id_s, kk > 0);
           }
-          mma_commit(bars.dp_full);
+          mma_commit_w(bars.dp_full);
           // dV(i) and S(i+1) are issued back to back once both can go: a wait
           // between two products would let the MMA queue run dry
-          if (!(ok = wait1(bars.p_full, gi & 1, wc, ERR_WAIT_MMA))) break;
+          if (!(ok = wait_warp(bars.p_full, gi & 1, wc, ERR_WAIT_MMA))) break;
           if (lt + 1 < n &&
-              !(ok = wait1(&bars.q_full[(gi + 1) & 1], ((gi + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
+              !(ok = wait_warp(&bars.q_full[(gi + 1) & 1], ((gi + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
             break;
           tc_fence_after();
           // dV += P^T dO  (P^T packed bf16: query columns [0,64) in TMEM columns
           // [0,32), [64,128) in [64,96))
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8, sdesc_offset(dsub, do_o + kk * 2048), id_acc,
+            mma_ts_w(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8, sdesc_offset(dsub, do_o + kk * 2048), id_acc,
                    (lt > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.do_empty[sd]);   // dV is the last reader of dO(i)
+          mma_commit_w(&bars.do_empty[sd]);   // dV is the last reader of dO(i)
           if (lt + 1 < n) issue_s(gi + 1);
-          if (!(ok = wait1(bars.ds_full, gi & 1, wc, ERR_WAIT_MMA))) break;
+          if (!(ok = wait_warp(bars.ds_full, gi & 1, wc, ERR_WAIT_MMA))) break;
           tc_fence_after();
           if constexpr (DET) {
             // dK += dS^T Q with dS^T packed in TMEM like P^T (in the dP^T columns)
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
-              mma_ts(t_dk, t_dp + (kk / 4) * 64 + (kk % 4) * 8, sdesc_offset(dsub, q_o + kk * 2048),
+              mma_ts_w(t_dk, t_dp + (kk / 4) * 64 + (kk % 4) * 8, sdesc_offset(dsub, q_o + kk * 2048),
                      id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&bars.q_empty[s]);
+            mma_commit_w(&bars.q_empty[s]);
           } else {
             // dQ = dS K, then dK += dS^T Q (A = dS^T: K-major view of the dS
             // boxes): dQ first, so that its read-out (which gates the next
             // dP) starts a product earlier
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
-              mma_ss(t_dp, sdesc_offset(dsub, C::OFF_DS + kk * 2048),
+              mma_ss_w(t_dp, sdesc_offset(dsub, C::OFF_DS + kk * 2048),
                      sdesc_offset(dsub, C::OFF_K + kk * 2048), id_dq, kk > 0 ? 1u : 0u);
-            mma_commit(bars.dq_full);
+            mma_commit_w(bars.dq_full);
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
-              mma_ss(t_dk, sdesc_offset(dk16, C::OFF_DS + (kk / 4) * C::SUB + (kk % 4) * 32),
+              mma_ss_w(t_dk, sdesc_offset(dk16, C::OFF_DS + (kk / 4) * C::SUB + (kk % 4) * 32),
                      sdesc_offset(dsub, q_o + kk * 2048), id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&bars.q_empty[s]);
+            mma_commit_w(&bars.q_empty[s]);
           }
         }
         // every MMA of this item: its K/V buffers are free, dK and dV final
-        mma_commit(bars.kv_empty);
+        mma_commit_w(bars.kv_empty);
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
       g += n;
       ++kph;
     }
-    if (lane == 0 && issued) {
-      mma_commit(bars.drain);
-      wait1(bars.drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
+    if (issued) {
+      mma_commit_w(bars.drain);
+      wait_warp(bars.drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
     }
   } else {
     // ================================================================ warps 0-7
@@ -809,7 +809,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       }
       // the tiles are written only if every warp staged its part (a warp
       // whose wait failed has raised the abort flag before arriving)
-      if (!cw_sync(u, 2) || !do_epi || *abort_flag) break;
+      // (the abort flag read once for the warp: its lanes leave together)
+      if (!cw_sync(u, 2) || !do_epi || __any_sync(0xffffffffu, *abort_flag)) break;
       const BwdItem t = bwd_item<CAUSAL>(a, cur->w);
       const bool ragged = p.cu_k != nullptr && t.key0 + kT > t.Nk;
       if (!ragged) {

@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     }
   } else if (warp == 9) {
     // ================================================================ MMA issuer
-    if (lane == 0 && n > 0) {
+    // (the whole warp, converged; lane 0 issues each instruction)
+    if (n > 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);   // S, dP (K-major)
       constexpr uint32_t id_dq = idesc_bf16_f32(kT, D, false, true);    // dQ: B = K, MN-major
       const uint32_t t_s = tmem, t_dp = tmem + 128, t_dq = tmem + 256;
@@ -239,14 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
-          mma_ts(d, a_t + kk * 8, sdesc_offset(dk16, b_o + o), id_s, kk > 0 ? 1u : 0u);
+          mma_ts_w(d, a_t + kk * 8, sdesc_offset(dk16, b_o + o), id_s, kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = wait1(qt_ready, 0, wc, ERR_WAIT_MMA) && wait1(&k_full[0], 0, wc, ERR_WAIT_MMA);
+      bool ok = wait_warp(qt_ready, 0, wc, ERR_WAIT_MMA) && wait_warp(&k_full[0], 0, wc, ERR_WAIT_MMA);
       if (ok) {
         tc_fence_after();
         issue_nt(t_s, t_q, C::OFF_K);
-        mma_commit(s_full);
+        mma_commit_w(s_full);
       }
       // Every wait of an iteration but the one for dS(i) comes first, while
       // dQ(i-1) is still executing, and dP(i), S(i+1) are then issued back to
@@ -255,34 +256,34 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       for (int i = 0; i < n && ok; ++i) {
         const int s = i % C::NSK, sv_ = i % C::NSV, s1 = (i + 1) % C::NSK;
         const bool next = i + 1 < n;
-        if (!(ok = wait1(&v_full[sv_], (i / C::NSV) & 1, wc, ERR_WAIT_MMA))) break;
+        if (!(ok = wait_warp(&v_full[sv_], (i / C::NSV) & 1, wc, ERR_WAIT_MMA))) break;
         // S(i+1) needs K_{i+1} and both warpgroups done reading S(i)
-        if (next && !(ok = wait1(&k_full[s1], ((i + 1) / C::NSK) & 1, wc, ERR_WAIT_MMA))) break;
-        if (next && !(ok = wait1(s_free, i & 1, wc, ERR_WAIT_MMA))) break;
+        if (next && !(ok = wait_warp(&k_full[s1], ((i + 1) / C::NSK) & 1, wc, ERR_WAIT_MMA))) break;
+        if (next && !(ok = wait_warp(s_free, i & 1, wc, ERR_WAIT_MMA))) break;
         tc_fence_after();
         // dP = dO V^T (the dP columns are free: dQ(i-1), which read dS(i-1)
         // there, was issued before and MMAs complete in order)
         issue_nt(t_dp, t_do, C::OFF_V + sv_ * C::TILE);
-        mma_commit(dp_full);
-        mma_commit(&v_empty[sv_]);
+        mma_commit_w(dp_full);
+        mma_commit_w(&v_empty[sv_]);
         if (next) {
           issue_nt(t_s, t_q, C::OFF_K + s1 * C::TILE);
-          mma_commit(s_full);
+          mma_commit_w(s_full);
         }
         // dQ += dS K_j: dS packed bf16, keys [0,64) in TMEM columns [128,160),
         // keys [64,128) in [192,224)
-        if (!(ok = wait1(ds_full, i & 1, wc, ERR_WAIT_MMA))) break;
+        if (!(ok = wait_warp(ds_full, i & 1, wc, ERR_WAIT_MMA))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ts(t_dq, t_dp + (kk / 4) * 64 + (kk % 4) * 8,
+          mma_ts_w(t_dq, t_dp + (kk / 4) * 64 + (kk % 4) * 8,
                  sdesc_offset(dsub, C::OFF_K + s * C::TILE + kk * 2048), id_dq,
                  (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&k_empty[s]);
+        mma_commit_w(&k_empty[s]);
       }
-      if (ok) mma_commit(dq_full);
-      mma_commit(drain);
-      wait1(drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
+      if (ok) mma_commit_w(dq_full);
+      mma_commit_w(drain);
+      wait_warp(drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
     }
   } else {
     // ================================================================ warps 0-7

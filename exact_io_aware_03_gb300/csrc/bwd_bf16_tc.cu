@@ -157,6 +157,16 @@ struct BwdCfg {
   static constexpr int TILE = kT * D * 2;     // bf16 [128][D]
   static constexpr int SUB = kT * 128;        // one 64-column box
   static constexpr int ND = DET ? 2 : 1;      // dO stages
+  // Threads and roles. Reduction form: warps 0-7 P and dS, 8-11 the dQ
+  // read-out (one per TMEM lane quarter), 12 TMA, 13 MMA, 14-15 idle (they
+  // complete the last warpgroup for the register split); deterministic
+  // form (no dQ): warps 0-7 P and dS, 8 TMA, 9 MMA.
+  static constexpr int NT = DET ? 320 : 512;
+  static constexpr int W_PROD = DET ? 8 : 12, W_MMA = DET ? 9 : 13;
+  // register split of the reduction form: the launch gives 512 x 128;
+  // warpgroups 0-2 take 144 each, warpgroup 3 (TMA, MMA, idle) gives up to 80
+  static constexpr int REG_HI = 144, REG_LO = 80;
+  static_assert(DET || 3 * 128 * REG_HI + 128 * REG_LO == 512 * 128, "register split");
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
   static constexpr int OFF_Q = OFF_V + TILE;         // [2 stages]
@@ -166,28 +176,42 @@ struct BwdCfg {
   // per Q stage: base-2 LSE [128] then D [128] of the tile's rows (TMA)
   static constexpr int OFF_STAT = OFF_DS + (DET ? 0 : kT * kT * 2);
   static constexpr int OFF_BAR = OFF_STAT + 2 * 2 * kT * 4;
-  static constexpr int NBAR = 2 + 2 + 2 + 2 * ND + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 2 + 2 + 1;
+  static constexpr int NBAR = 18 + 2 * ND;   // see BwdBars
   static constexpr int OFF_SCALARS = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_SCALARS + 16 + 2 * 48;   // flags, then the work-item ring
 };
 
+// The kernel's mbarriers: one array in shared memory, each barrier at a fixed
+// index (addresses computed at each use from the one base, rather than kept
+// as separate pointers across the whole kernel).
+template <int ND>
 struct BwdBars {
-  uint64_t* kv_full;   // K, V of the current item landed
-  uint64_t* kv_empty;  // every MMA of an item done (its K/V free, dK and dV final)
-  uint64_t* q_full;    // [2]  Q_i and its base-2 LSE and D of a stage
-  uint64_t* q_empty;   // [2]
-  uint64_t* do_full;   // [ND] dO_i
-  uint64_t* do_empty;  // [ND]
-  uint64_t* s_full;    // S^T done
-  uint64_t* dp_full;   // dP^T done
-  uint64_t* p_full;    // P^T in TMEM (one arrival per compute warp)
-  uint64_t* ds_full;   // dS^T in TMEM + smem (one arrival per compute warp)
-  uint64_t* dq_full;   // dQ_i done (and everything before it); DET: the last dK done
-  uint64_t* dq_empty;  // dQ_i read out of TMEM (one arrival per compute warp)
-  uint64_t* drain;     // every MMA of the CTA done (the MMA warp's final commit)
-  uint64_t* sched_full;    // [2] work-item ring: item index written
-  uint64_t* sched_empty;   // [2] read by the MMA thread and every compute warp
-  uint64_t* cw;        // barrier of the compute warps (one arrival per warp)
+  uint64_t* b;
+  // K, V of the current item landed / every MMA of an item done (its K/V
+  // free, dK and dV final)
+  __device__ __forceinline__ uint64_t* kv_full() const { return b; }
+  __device__ __forceinline__ uint64_t* kv_empty() const { return b + 1; }
+  // [2] Q_i with its statistics in a stage / the stage free
+  __device__ __forceinline__ uint64_t* q_full() const { return b + 2; }
+  __device__ __forceinline__ uint64_t* q_empty() const { return b + 4; }
+  // [ND] dO_i landed / free
+  __device__ __forceinline__ uint64_t* do_full() const { return b + 6; }
+  __device__ __forceinline__ uint64_t* do_empty() const { return b + 6 + ND; }
+  // S^T done; dP^T done; P^T in TMEM, dS^T written (one arrival per P/dS
+  // warp); dQ_i done; dQ_i read out of TMEM (one arrival per dQ warp);
+  // every MMA of the CTA done
+  __device__ __forceinline__ uint64_t* s_full() const { return b + 6 + 2 * ND; }
+  __device__ __forceinline__ uint64_t* dp_full() const { return b + 7 + 2 * ND; }
+  __device__ __forceinline__ uint64_t* p_full() const { return b + 8 + 2 * ND; }
+  __device__ __forceinline__ uint64_t* ds_full() const { return b + 9 + 2 * ND; }
+  __device__ __forceinline__ uint64_t* dq_full() const { return b + 10 + 2 * ND; }
+  __device__ __forceinline__ uint64_t* dq_empty() const { return b + 11 + 2 * ND; }
+  __device__ __forceinline__ uint64_t* drain() const { return b + 12 + 2 * ND; }
+  // [2] work-item ring: item written / read by every consumer warp
+  __device__ __forceinline__ uint64_t* sched_full() const { return b + 13 + 2 * ND; }
+  __device__ __forceinline__ uint64_t* sched_empty() const { return b + 15 + 2 * ND; }
+  // barrier of the P/dS warps (one arrival per warp)
+  __device__ __forceinline__ uint64_t* cw() const { return b + 17 + 2 * ND; }
 };
 
 
@@ -274,7 +298,7 @@ __device__ __forceinline__ bool bwd_item_any_key(const BwdBf16Args& a, const Bwd
 // warps write out the previous item's dK and dV. The deterministic form
 // (dS^T through TMEM, no dQ) takes one item per CTA, the CTA's index.
 template <int D, bool CAUSAL, bool BIAS, bool DET>
-__global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdBf16Args a) {
+__global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const __grid_constant__ BwdBf16Args a) {
   using C = BwdCfg<D, DET>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const Problem& p = a.p;
@@ -282,23 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   const int lane = threadIdx.x & 31;
 
   uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  BwdBars bars;
-  bars.kv_full = bb; bb += 1;
-  bars.kv_empty = bb; bb += 1;
-  bars.q_full = bb; bb += 2;
-  bars.q_empty = bb; bb += 2;
-  bars.do_full = bb; bb += C::ND;
-  bars.do_empty = bb; bb += C::ND;
-  bars.s_full = bb; bb += 1;
-  bars.dp_full = bb; bb += 1;
-  bars.p_full = bb; bb += 1;
-  bars.ds_full = bb; bb += 1;
-  bars.dq_full = bb; bb += 1;
-  bars.dq_empty = bb; bb += 1;
-  bars.drain = bb; bb += 1;
-  bars.sched_full = bb; bb += 2;
-  bars.sched_empty = bb; bb += 2;
-  bars.cw = bb;
+  const BwdBars<C::ND> bars{reinterpret_cast<uint64_t*>(smem + C::OFF_BAR)};
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_SCALARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SCALARS + 4);
   volatile BwdSlot* slots = reinterpret_cast<volatile BwdSlot*>(smem + C::OFF_SCALARS + 16);   // [2]
@@ -307,30 +315,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     if ((smem_u32(smem) & 1023u) != 0) atomicOr(a.err, ERR_WAIT_DRAIN);   // layout invariant
-    mbar_init(bars.kv_full, 1);
-    mbar_init(bars.kv_empty, 1);
+    mbar_init(bars.kv_full(), 1);
+    mbar_init(bars.kv_empty(), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars.q_full[s], 1);
-      mbar_init(&bars.q_empty[s], 1);
-      mbar_init(&bars.sched_full[s], 1);
-      mbar_init(&bars.sched_empty[s], 1 + 2 * kT / 32);   // the MMA thread + each compute warp
+      mbar_init(&bars.q_full()[s], 1);
+      mbar_init(&bars.q_empty()[s], 1);
+      mbar_init(&bars.sched_full()[s], 1);
+      // the MMA warp, each P/dS warp and each dQ warp
+      mbar_init(&bars.sched_empty()[s], 1 + 2 * kT / 32 + (DET ? 0 : 4));
     }
     for (int s = 0; s < C::ND; ++s) {
-      mbar_init(&bars.do_full[s], 1);
-      mbar_init(&bars.do_empty[s], 1);
+      mbar_init(&bars.do_full()[s], 1);
+      mbar_init(&bars.do_empty()[s], 1);
     }
-    mbar_init(bars.s_full, 1);
-    mbar_init(bars.dp_full, 1);
-    mbar_init(bars.p_full, 2 * kT / 32);    // one arrival per compute warp
-    mbar_init(bars.ds_full, 2 * kT / 32);
-    mbar_init(bars.dq_full, 1);
-    mbar_init(bars.dq_empty, 2 * kT / 32);
-    mbar_init(bars.drain, 1);
-    mbar_init(bars.cw, 2 * kT / 32);
+    mbar_init(bars.s_full(), 1);
+    mbar_init(bars.dp_full(), 1);
+    mbar_init(bars.p_full(), 2 * kT / 32);    // one arrival per compute warp
+    mbar_init(bars.ds_full(), 2 * kT / 32);
+    mbar_init(bars.dq_full(), 1);
+    mbar_init(bars.dq_empty(), 4);            // one arrival per dQ warp
+    mbar_init(bars.drain(), 1);
+    mbar_init(bars.cw(), 2 * kT / 32);
     *abort_flag = (smem_u32(smem) & 1023u) != 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == C::W_MMA) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -345,7 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   auto q_coord = [&](const BwdItem& t, int h) { return p.cu_q ? h : t.b * p.H + h; };
   auto q_row0 = [&](const BwdItem& t, int lt) { return (t.i0 + lt % max(t.nqh, 1)) * kT; };
 
-  if (warp == 8) {
+  if (warp >= C::W_PROD) {
+  if constexpr (!DET) setmaxnreg_dec<C::REG_LO>();
+  if (warp == C::W_PROD) {
     // ================================================================ TMA producer + scheduler
     int g = 0, kph = 0;     // query-tile steps / non-empty items so far
     int nq = 0, nd = 0, nkv = 0;   // Q / dO / K,V fills issued
@@ -367,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       }
       if (lane == 0) {
         // slot u & 1 is free once item u - 2 is done with it
-        if (u >= 2 && !wait1(&bars.sched_empty[u & 1], ((u >> 1) - 1) & 1, wc, ERR_WAIT_LOAD)) ok = false;
+        if (u >= 2 && !wait1(&bars.sched_empty()[u & 1], ((u >> 1) - 1) & 1, wc, ERR_WAIT_LOAD)) ok = false;
         if (ok) {
           volatile BwdSlot* sl = slots + (u & 1);
           sl->w = w;
@@ -384,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             sl->g0 = g;
             sl->kph = kph;
           }
-          mbar_arrive(&bars.sched_full[u & 1]);
+          mbar_arrive(&bars.sched_full()[u & 1]);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -392,37 +403,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       if (n == 0) continue;
       if (lane == 0 && !*abort_flag) {
         // K and V of the previous item are free once all of its MMAs are done
-        if (kph > 0 && !wait1(bars.kv_empty, (kph - 1) & 1, wc, ERR_WAIT_LOAD)) ok = false;
+        if (kph > 0 && !wait1(bars.kv_empty(), (kph - 1) & 1, wc, ERR_WAIT_LOAD)) ok = false;
         if (ok) {
-          mbar_arrive_expect_tx(bars.kv_full, 2 * C::TILE);
+          mbar_arrive_expect_tx(bars.kv_full(), 2 * C::TILE);
           for (int c = 0; c < D / 64; ++c) {
             tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, t.sv.k_off + t.key0, t.sv.hk,
-                        bars.kv_full);
+                        bars.kv_full());
             tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, t.sv.k_off + t.key0, t.sv.hk,
-                        bars.kv_full);
+                        bars.kv_full());
           }
           ++nkv;
         }
         for (int lt = 0; lt < n && ok; ++lt) {
           const int gi = g + lt, s = gi & 1, uq = gi >> 1;
           const int q0 = q_row0(t, lt), hq = q_head(t, lt);
-          if (uq > 0 && !wait1(&bars.q_empty[s], (uq - 1) & 1, wc, ERR_WAIT_LOAD)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars.q_full[s], C::TILE + 2 * kT * 4);
+          if (uq > 0 && !wait1(&bars.q_empty()[s], (uq - 1) & 1, wc, ERR_WAIT_LOAD)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars.q_full()[s], C::TILE + 2 * kT * 4);
           for (int c = 0; c < D / 64; ++c)
             tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * C::SUB, &a.tm_q, c * 64,
-                        t.sv.q_off + q0, q_coord(t, hq), &bars.q_full[s]);
+                        t.sv.q_off + q0, q_coord(t, hq), &bars.q_full()[s]);
           float* st = reinterpret_cast<float*>(smem + C::OFF_STAT) + s * 2 * kT;
           const size_t srow = ((size_t)t.b * p.H + hq) * a.nq_pad + q0;
-          bulk_load_1d(st, a.lse2 + srow, kT * 4, &bars.q_full[s]);
-          bulk_load_1d(st + kT, a.D + srow, kT * 4, &bars.q_full[s]);
+          bulk_load_1d(st, a.lse2 + srow, kT * 4, &bars.q_full()[s]);
+          bulk_load_1d(st + kT, a.D + srow, kT * 4, &bars.q_full()[s]);
           ++nq;
           // dO stage sd may be refilled once dV of its previous tile is done
           const int sd = gi % C::ND, ud = gi / C::ND;
-          if (ud > 0 && !wait1(&bars.do_empty[sd], (ud - 1) & 1, wc, ERR_WAIT_LOAD)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars.do_full[sd], C::TILE);
+          if (ud > 0 && !wait1(&bars.do_empty()[sd], (ud - 1) & 1, wc, ERR_WAIT_LOAD)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars.do_full()[sd], C::TILE);
           for (int c = 0; c < D / 64; ++c)
             tma_load_3d(smem + C::OFF_DO + sd * C::TILE + c * C::SUB, &a.tm_do, c * 64,
-                        t.sv.q_off + q0, q_coord(t, hq), &bars.do_full[sd]);
+                        t.sv.q_off + q0, q_coord(t, hq), &bars.do_full()[sd]);
           ++nd;
         }
       }
@@ -434,12 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       // Drain: wait (bounded, ignoring the abort flag) for the last fill of
       // every buffer, so that no copy is still landing when the CTA exits.
       const WaitCtx wd{abort_flag, a.err, true};
-      if (nkv > 0) wait1(bars.kv_full, (nkv - 1) & 1, wd, ERR_WAIT_DRAIN);
-      for (int i = max(0, nq - 2); i < nq; ++i) wait1(&bars.q_full[i & 1], (i >> 1) & 1, wd, ERR_WAIT_DRAIN);
+      if (nkv > 0) wait1(bars.kv_full(), (nkv - 1) & 1, wd, ERR_WAIT_DRAIN);
+      for (int i = max(0, nq - 2); i < nq; ++i) wait1(&bars.q_full()[i & 1], (i >> 1) & 1, wd, ERR_WAIT_DRAIN);
       for (int i = max(0, nd - C::ND); i < nd; ++i)
-        wait1(&bars.do_full[i % C::ND], (i / C::ND) & 1, wd, ERR_WAIT_DRAIN);
+        wait1(&bars.do_full()[i % C::ND], (i / C::ND) & 1, wd, ERR_WAIT_DRAIN);
     }
-  } else if (warp == 9) {
+  } else if (warp == C::W_MMA) {
     // ================================================================ MMA issuer
     constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);    // S^T, dP^T
     constexpr uint32_t id_acc = idesc_bf16_f32(kT, D, false, true);    // dV, dK (A K-major)
@@ -449,24 +460,32 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // operand's is this plus its byte offset (K-major boxes read along K:
     // LBO 16; along the 128-row direction: LBO = one box)
     const uint32_t sbase = smem_u32(smem);
-    const uint64_t dk16 = sdesc_sw128(sbase, 16, 1024), dsub = sdesc_sw128(sbase, C::SUB, 1024);
+    const uint64_t dk16c = sdesc_sw128(sbase, 16, 1024), dsubc = sdesc_sw128(sbase, C::SUB, 1024);
+    // the bases passed through an opaque move inside each step, so that the
+    // forty descriptors of a step are one add each right where they are
+    // used, not values kept in registers across the loop
+    auto opaque = [](uint64_t x) {
+      asm volatile("" : "+l"(x));
+      return x;
+    };
     // S^T = K Q^T for global step gi (both K-major, 128-byte rows per box)
     auto issue_s = [&](int gi) {
       const uint32_t q_o = C::OFF_Q + (gi & 1) * C::TILE;
+      const uint64_t dk16 = opaque(dk16c);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
         mma_ss_w(t_s, sdesc_offset(dk16, C::OFF_K + o), sdesc_offset(dk16, q_o + o), id_s, kk > 0);
       }
-      mma_commit_w(bars.s_full);
+      mma_commit_w(bars.s_full());
     };
     int g = 0, kph = 0;
     bool ok = true, issued = false;
     for (int u = 0; ok; ++u) {
-      if (!wait_warp(&bars.sched_full[u & 1], (u >> 1) & 1, wc, ERR_WAIT_LOAD)) break;
+      if (!wait_warp(&bars.sched_full()[u & 1], (u >> 1) & 1, wc, ERR_WAIT_LOAD)) break;
       const int w = slots[u & 1].w, n = slots[u & 1].n;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.sched_empty[u & 1]);
+      if (lane == 0) mbar_arrive(&bars.sched_empty()[u & 1]);
       if (w < 0) break;
       if (n == 0) continue;
       {
@@ -477,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         // of tile i+1 thus overlap dQ(i) and dK(i). The first dV and dK of
         // an item start from zero: the P/dS warps arrive on P of the item's
         // first tile only after they have read the previous item's dK, dV.
-        ok = !__any_sync(0xffffffffu, *abort_flag) && wait_warp(bars.kv_full, kph & 1, wc, ERR_WAIT_MMA) &&
-             wait_warp(&bars.q_full[g & 1], (g >> 1) & 1, wc, ERR_WAIT_MMA);
+        ok = !__any_sync(0xffffffffu, *abort_flag) && wait_warp(bars.kv_full(), kph & 1, wc, ERR_WAIT_MMA) &&
+             wait_warp(&bars.q_full()[g & 1], (g >> 1) & 1, wc, ERR_WAIT_MMA);
         if (ok) {
           tc_fence_after();
           issue_s(g);
@@ -487,23 +506,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         for (int lt = 0; lt < n && ok; ++lt) {
           const int gi = g + lt, s = gi & 1, sd = gi % C::ND;
           const uint32_t q_o = C::OFF_Q + s * C::TILE, do_o = C::OFF_DO + sd * C::TILE;
+          const uint64_t dk16 = opaque(dk16c), dsub = opaque(dsubc);
           // dP^T = V dO^T, once dQ of the previous tile has left TMEM (DET: the
           // dS^T of the previous tile in these columns was read by dK, an
           // earlier MMA)
-          if (!DET && gi > 0 && !(ok = wait_warp(bars.dq_empty, (gi - 1) & 1, wc, ERR_WAIT_MMA))) break;
-          if (!(ok = wait_warp(&bars.do_full[sd], (gi / C::ND) & 1, wc, ERR_WAIT_MMA))) break;
+          if (!DET && gi > 0 && !(ok = wait_warp(bars.dq_empty(), (gi - 1) & 1, wc, ERR_WAIT_MMA))) break;
+          if (!(ok = wait_warp(&bars.do_full()[sd], (gi / C::ND) & 1, wc, ERR_WAIT_MMA))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = (kk / 4) * C::SUB + (kk % 4) * 32;
             mma_ss_w(t_dp, sdesc_offset(dk16, C::OFF_V + o), sdesc_offset(dk16, do_o + o), id_s, kk > 0);
           }
-          mma_commit_w(bars.dp_full);
+          mma_commit_w(bars.dp_full());
           // dV(i) and S(i+1) are issued back to back once both can go: a wait
           // between two products would let the MMA queue run dry
-          if (!(ok = wait_warp(bars.p_full, gi & 1, wc, ERR_WAIT_MMA))) break;
+          if (!(ok = wait_warp(bars.p_full(), gi & 1, wc, ERR_WAIT_MMA))) break;
           if (lt + 1 < n &&
-              !(ok = wait_warp(&bars.q_full[(gi + 1) & 1], ((gi + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
+              !(ok = wait_warp(&bars.q_full()[(gi + 1) & 1], ((gi + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
             break;
           tc_fence_after();
           // dV += P^T dO  (P^T packed bf16: query columns [0,64) in TMEM columns
@@ -512,9 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           for (int kk = 0; kk < kT / 16; ++kk)
             mma_ts_w(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8, sdesc_offset(dsub, do_o + kk * 2048), id_acc,
                    (lt > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_w(&bars.do_empty[sd]);   // dV is the last reader of dO(i)
+          mma_commit_w(&bars.do_empty()[sd]);   // dV is the last reader of dO(i)
           if (lt + 1 < n) issue_s(gi + 1);
-          if (!(ok = wait_warp(bars.ds_full, gi & 1, wc, ERR_WAIT_MMA))) break;
+          if (!(ok = wait_warp(bars.ds_full(), gi & 1, wc, ERR_WAIT_MMA))) break;
           tc_fence_after();
           if constexpr (DET) {
             // dK += dS^T Q with dS^T packed in TMEM like P^T (in the dP^T columns)
@@ -522,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             for (int kk = 0; kk < kT / 16; ++kk)
               mma_ts_w(t_dk, t_dp + (kk / 4) * 64 + (kk % 4) * 8, sdesc_offset(dsub, q_o + kk * 2048),
                      id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
-            mma_commit_w(&bars.q_empty[s]);
+            mma_commit_w(&bars.q_empty()[s]);
           } else {
             // dQ = dS K, then dK += dS^T Q (A = dS^T: K-major view of the dS
             // boxes): dQ first, so that its read-out (which gates the next
@@ -531,90 +551,102 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             for (int kk = 0; kk < kT / 16; ++kk)
               mma_ss_w(t_dp, sdesc_offset(dsub, C::OFF_DS + kk * 2048),
                      sdesc_offset(dsub, C::OFF_K + kk * 2048), id_dq, kk > 0 ? 1u : 0u);
-            mma_commit_w(bars.dq_full);
+            mma_commit_w(bars.dq_full());
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
               mma_ss_w(t_dk, sdesc_offset(dk16, C::OFF_DS + (kk / 4) * C::SUB + (kk % 4) * 32),
                      sdesc_offset(dsub, q_o + kk * 2048), id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
-            mma_commit_w(&bars.q_empty[s]);
+            mma_commit_w(&bars.q_empty()[s]);
           }
         }
         // every MMA of this item: its K/V buffers are free, dK and dV final
-        mma_commit_w(bars.kv_empty);
+        mma_commit_w(bars.kv_empty());
       }
       g += n;
       ++kph;
     }
     if (issued) {
-      mma_commit_w(bars.drain);
-      wait_warp(bars.drain, 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
+      mma_commit_w(bars.drain());
+      wait_warp(bars.drain(), 0, WaitCtx{abort_flag, a.err, true}, ERR_WAIT_DRAIN);
     }
+  }
+  } else if (!DET && warp >= 8) {
+    // ================================================================ dQ warps 8-11
+    setmaxnreg_inc<C::REG_HI>();
+    // dQ of every query-tile step (TMEM lane = query row): each warp reads its
+    // 32 rows, all D columns, out of TMEM at once (the columns go back to the
+    // MMA warp for the next dP), then reduce-adds them into the fp32
+    // accumulator with TMA in boxes of 32 rows x 32 columns (4 KiB, 128-byte
+    // swizzled), two at a time through its 8 KiB slot of the staging buffer.
+    const int qw = warp - 8;   // TMEM lane quarter
+    const uint32_t lane_base = tmem + ((uint32_t)(qw * 32) << 16);
+    uint8_t* slot = smem + C::OFF_DQST + qw * 8192;
+    constexpr int NB = D / 32;   // boxes per row block
+    for (int u = 0;; ++u) {
+      if (!wait_warp(&bars.sched_full()[u & 1], (u >> 1) & 1, wc, ERR_WAIT_LOAD)) break;
+      volatile BwdSlot* cur = slots + (u & 1);
+      if (cur->w < 0) break;
+      const int n = cur->n, g = cur->g0;
+      bool ok = true;
+      for (int lt = 0; lt < n && ok; ++lt) {
+        const int gi = g + lt;
+        if (!(ok = wait_warp(bars.dq_full(), gi & 1, wc, ERR_WAIT_EPILOGUE))) break;
+        tc_fence_after();
+        uint32_t x[D];
+#pragma unroll
+        for (int c = 0; c < D; c += 32) tmem_ld32(lane_base + 128 + c, x + c);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive_warp(bars.dq_empty());
+        const int nqh = cur->nqh;
+        const int row0 = cur->q_off + (cur->i0 + lt % nqh) * kT + qw * 32;
+        const int qc = cur->qc0 + lt / nqh;
+#pragma unroll
+        for (int b2 = 0; b2 < NB; b2 += 2) {
+          if (lane == 0) bulk_wait_group_read0();   // the slot's previous boxes have been read
+          __syncwarp();
+#pragma unroll
+          for (int bb = 0; bb < 2; ++bb) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t* v = x + (b2 + bb) * 32 + 4 * k;
+              *reinterpret_cast<uint4*>(slot + bb * 4096 + lane * 128 + ((k ^ (lane & 7)) * 16)) =
+                  make_uint4(v[0], v[1], v[2], v[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int bb = 0; bb < 2; ++bb)
+              tma_reduce_add_3d(&a.tm_dqacc, slot + bb * 4096, (b2 + bb) * 32, row0, qc);
+            bulk_commit_group();
+          }
+        }
+      }
+      mbar_arrive_warp(&bars.sched_empty()[u & 1]);   // done with the slot
+      if (!ok) break;
+    }
+    // reductions complete before the CTA exits
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   } else {
     // ================================================================ warps 0-7
+    if constexpr (!DET) setmaxnreg_inc<C::REG_HI>();
     // Two warpgroups share the 128 keys (thread = key = TMEM lane) and split the
     // 128 query columns of each tile: warpgroup h handles columns [64h, 64h+64)
-    // of S^T / P^T / dP^T / dS^T, and columns [h*D/2, (h+1)*D/2) of dQ, dK, dV.
+    // of S^T / P^T / dP^T / dS^T, and columns [h*D/2, (h+1)*D/2) of dK, dV.
     const int h = warp / 4;
     const int r = (warp % 4) * 32 + lane;            // key within the tile = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const float sl2 = p.scale * kLog2e;
     float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);
     uint8_t* ds_s = smem + C::OFF_DS;
-    constexpr int HD = D / 2;      // dQ / dK / dV columns per warpgroup
+    constexpr int HD = D / 2;      // dK / dV columns per warpgroup
     // the current item: its ring slot (read from shared memory where needed,
     // to keep the tile loop's registers few) and first global step
     volatile BwdSlot* cur = slots;
 
-    // dQ of global step gi (TMEM lane = query row): this warpgroup's columns
-    // are read out of TMEM at once (the columns go back to the MMA warp)
-    // and reduce-added into the fp32 accumulator with TMA in boxes
-    // of 32 rows x 32 columns (4 KiB, 128-byte swizzled) staged in this
-    // warp's slot of the staging buffer. A TMA reduction reads its box at
-    // ~25 B/clock, so a warp stages its first box right away and keeps the
-    // second in registers until after the next tile's dS (by then the first
-    // box has been read): nothing waits on the reductions, and the dS
-    // buffer is never used for staging.
-    uint8_t* dq_stage = smem + C::OFF_DQST + warp * 4096;
-    uint32_t dq_hold[32];   // second box of the pending dQ (d = 128)
-    auto stage_box = [&](const uint32_t* v32, int col, int row0, int qc) {
-      if (lane == 0) bulk_wait_group_read0();   // the previous box has been read
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t* v = v32 + 4 * k;
-        *reinterpret_cast<uint4*>(dq_stage + lane * 128 + ((k ^ (lane & 7)) * 16)) =
-            make_uint4(v[0], v[1], v[2], v[3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_reduce_add_3d(&a.tm_dqacc, dq_stage, col, row0, qc);
-        bulk_commit_group();
-      }
-    };
-    auto dq_readout = [&](int gi) -> bool {
-      if (!wait_warp(bars.dq_full, gi & 1, wc, ERR_WAIT_EPILOGUE)) return false;
-      tc_fence_after();
-      uint32_t x[32];
-      tmem_ld32(lane_base + 128 + h * HD, x);
-      if constexpr (HD > 32) tmem_ld32(lane_base + 128 + h * HD + 32, dq_hold);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive_warp(bars.dq_empty);
-      const int lt = gi - cur->g0, nqh = cur->nqh;
-      stage_box(x, h * HD, cur->q_off + (cur->i0 + lt % nqh) * kT + (warp % 4) * 32,
-                cur->qc0 + lt / nqh);
-      return true;
-    };
-    // the second box of the pending dQ of global step gi (no-op at d = 64,
-    // which has one)
-    auto dq_finish = [&](int gi) {
-      if constexpr (HD > 32) {
-        const int lt = gi - cur->g0, nqh = cur->nqh;
-        stage_box(dq_hold, h * HD + 32, cur->q_off + (cur->i0 + lt % nqh) * kT + (warp % 4) * 32,
-                  cur->qc0 + lt / nqh);
-      }
-    };
     // P^T of global step gi = exp2(S^T * scale*log2e + bias - LSE2), masked
     // -> 0, kept in fp32 registers for dS; packed bf16 copy to TMEM for dV.
     float P[64];
@@ -622,9 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       const int q0 = (cur->i0 + (gi - cur->g0) % cur->nqh) * kT;
       const int off = cur->off, key = cur->key0 + r;
       // this tile's base-2 LSE (staged by TMA with Q) for this warpgroup's columns
-      if (!wait_warp(&bars.q_full[gi & 1], (gi >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) return false;
+      if (!wait_warp(&bars.q_full()[gi & 1], (gi >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       const float* stl = stat + (gi & 1) * 2 * kT + h * 64;
-      if (!wait_warp(bars.s_full, gi & 1, wc, ERR_WAIT_SOFTMAX)) return false;
+      if (!wait_warp(bars.s_full(), gi & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
       const bool need_mask = CAUSAL && (q0 + off < key - r + kT - 1);
       // the key's term: its bias (log2 domain), -inf past the end of a ragged tile
@@ -661,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive_warp(bars.p_full);
+      mbar_arrive_warp(bars.p_full());
       return true;
     };
     // dS^T = scale * P^T o (dP^T - D) of global step gi, into the dS boxes
@@ -669,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     auto compute_ds = [&](int gi) -> bool {
       const float* std_ = stat + (gi & 1) * 2 * kT + kT + h * 64;   // -scale * D
       const uint64_t sc2 = f2_pack(p.scale, p.scale);
-      if (!wait_warp(bars.dp_full, gi & 1, wc, ERR_WAIT_SOFTMAX)) return false;
+      if (!wait_warp(bars.dp_full(), gi & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
       // two chunks of 32 query columns, to keep the live registers low
 #pragma unroll
@@ -716,39 +748,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive_warp(bars.ds_full);
+      mbar_arrive_warp(bars.ds_full());
       return true;
     };
 
     // The staging of dK and dV: the Q stages in the deterministic form (one
-    // item per CTA: free once its MMAs are done); otherwise the dQ staging
-    // and dS buffers (64 KiB together), whose next writers wait until TMA
-    // has read the staging, so the next item's loads are not held up.
-    uint8_t* stage = DET ? smem + C::OFF_Q : smem + C::OFF_DQST;   // [dV, dK][D/64 boxes][128 keys][128 B]
+    // item per CTA: free once its MMAs are done); otherwise the dS buffer,
+    // in two rounds (dV, then dK) at d = 128, whose next writers wait until
+    // TMA has read the staging, so the next item's loads are not held up.
+    uint8_t* stage = DET ? smem + C::OFF_Q : smem + C::OFF_DS;   // [D/64 boxes][128 keys][128 B] per tensor
+    constexpr int ROUNDS = (!DET && 2 * C::TILE > 32768) ? 2 : 1;
+    constexpr int PER = 2 / ROUNDS;   // tensors staged per round
     // barrier of the eight compute warps, on an mbarrier so that a warp that
-    // has stopped makes the others' wait run out instead of hang. Use j of
-    // item u (j = 0..2, the first only for u > 0) is its phase 3u - 1 + j.
+    // has stopped makes the others' wait run out instead of hang. Item u
+    // uses it 1 + 2 * ROUNDS times (the first use, j = 0, only for u > 0);
+    // use j of item u is phase U u - 1 + j.
+    constexpr int U = 1 + 2 * ROUNDS;
     auto cw_sync = [&](int u, int j) -> bool {
-      mbar_arrive_warp(bars.cw);
-      return wait_warp(bars.cw, (3 * u - 1 + j) & 1, wc, ERR_WAIT_EPILOGUE);
+      mbar_arrive_warp(bars.cw());
+      return wait_warp(bars.cw(), (U * u - 1 + j) & 1, wc, ERR_WAIT_EPILOGUE);
     };
     for (int u = 0;; ++u) {
-      if (!wait_warp(&bars.sched_full[u & 1], (u >> 1) & 1, wc, ERR_WAIT_LOAD)) break;
+      if (!wait_warp(&bars.sched_full()[u & 1], (u >> 1) & 1, wc, ERR_WAIT_LOAD)) break;
       cur = slots + (u & 1);   // held until this item's epilogue is done with it
       if (cur->w < 0) break;
       const int n = cur->n;
 
-      // Order per tile i: dS(i), the second dQ box of tile i-1, P(i+1) (its
-      // S^T was issued right after dV(i)), then the read-out of dQ(i); P of
-      // the item's first tile first.
+      // Order per tile i: dS(i), then P(i+1) (its S^T was issued right after
+      // dV(i)); P of the item's first tile first.
       bool ok = true;
       int lt = 0;
       const int g = cur->g0;
       if (n > 0) ok = compute_p(g);
       if (u > 0) {
         // every compute warp passes here once per item, even after a failed
-        // wait: the previous item's dK/dV staging (the dS and dQ staging
-        // buffers) has been read by TMA before anything writes them again
+        // wait: the previous item's dK/dV staging has been read by TMA
+        // before anything writes it again
         if (!DET && threadIdx.x == 0) bulk_wait_group_read0();
         if (!cw_sync(u, 0)) ok = false;
       }
@@ -756,14 +791,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         for (; ok && lt < n; ++lt) {
           const int gi = g + lt;
           if (!(ok = compute_ds(gi))) break;
-          if (!DET && lt > 0) dq_finish(gi - 1);
           if (lt + 1 < n && !(ok = compute_p(gi + 1))) break;
-          if (!DET && !(ok = dq_readout(gi))) break;
         }
         if (ok) {
-          if (!DET) dq_finish(g + n - 1);
           // every MMA of the item is done (the last dK follows the last dQ)
-          ok = wait_warp(bars.kv_empty, cur->kph & 1, wc, ERR_WAIT_EPILOGUE);
+          ok = wait_warp(bars.kv_empty(), cur->kph & 1, wc, ERR_WAIT_EPILOGUE);
           tc_fence_after();
         }
       }
@@ -772,81 +804,92 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       // memory as the 128-byte-swizzled 64-column boxes TMA uses; one thread
       // then stores the tiles with TMA. A packed sequence's ragged last tile
       // is written with plain coalesced stores instead (a 128-row box would
-      // run into the next sequence's rows). Every compute warp reaches both
-      // barriers once per item.
-      if (!DET && lane == 0) bulk_wait_group_read0();   // this warp's dQ boxes have been read
-      if (!cw_sync(u, 1)) ok = false;                    // ... and every other warp's
-      const bool do_epi = ok;
-      if (do_epi) {
-        const bool have = n > 0;
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {   // 0: dV, 1: dK
-#pragma unroll
-          for (int c0 = 0; c0 < HD; c0 += 32) {
-            uint32_t x[32];
-            if (have) {
-              tmem_ld32(lane_base + 256 + which * D + h * HD + c0, x);
-              tmem_ld_wait();
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) x[e] = 0u;
-            }
-            uint32_t pkd[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
-            const int col = h * HD + c0;   // first column of these 32
-            uint8_t* rowp = stage + which * C::TILE + (col / 64) * C::SUB + r * 128;
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              const int j = (col % 64) / 8 + v4;
-              *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) * 16)) =
-                  make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
-            }
-          }
-        }
-        fence_proxy_async_smem();   // the generic-proxy writes, before TMA reads them
-      }
-      // the tiles are written only if every warp staged its part (a warp
-      // whose wait failed has raised the abort flag before arriving)
-      // (the abort flag read once for the warp: its lanes leave together)
-      if (!cw_sync(u, 2) || !do_epi || __any_sync(0xffffffffu, *abort_flag)) break;
+      // run into the next sequence's rows). Every compute warp reaches each
+      // barrier once per item.
       const BwdItem t = bwd_item<CAUSAL>(a, cur->w);
       const bool ragged = p.cu_k != nullptr && t.key0 + kT > t.Nk;
-      if (!ragged) {
-        if (threadIdx.x == 0) {
+      bool stop = false;
 #pragma unroll
-          for (int which = 0; which < 2; ++which)
+      for (int rd = 0; rd < ROUNDS; ++rd) {
+        // the staging is free: the item's MMAs are done (each warp waited)
+        // and the previous round's (or item's) staging has been read
+        if (rd > 0 && threadIdx.x == 0) bulk_wait_group_read0();
+        if (!cw_sync(u, 1 + 2 * rd)) ok = false;
+        const bool do_epi = ok;
+        if (do_epi) {
+          const bool have = n > 0;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-              tma_store_3d(which ? &a.tm_dk : &a.tm_dv, stage + which * C::TILE + c * C::SUB,
-                           c * 64, t.sv.k_off + t.key0, t.sv.hk);
-          bulk_commit_group();
+          for (int wl = 0; wl < PER; ++wl) {
+            const int which = rd * PER + wl;   // 0: dV, 1: dK
+#pragma unroll
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+              uint32_t x[32];
+              if (have) {
+                tmem_ld32(lane_base + 256 + which * D + h * HD + c0, x);
+                tmem_ld_wait();
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[e] = 0u;
+              }
+              uint32_t pkd[16];
+#pragma unroll
+              for (int e = 0; e < 32; e += 2)
+                pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+              const int col = h * HD + c0;   // first column of these 32
+              uint8_t* rowp = stage + wl * C::TILE + (col / 64) * C::SUB + r * 128;
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                const int j = (col % 64) / 8 + v4;
+                *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) * 16)) =
+                    make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+              }
+            }
+          }
+          fence_proxy_async_smem();   // the generic-proxy writes, before TMA reads them
         }
-      } else {
-        constexpr int CPR = D / 8;   // 16-byte pieces per row
-        for (int idx = threadIdx.x; idx < 2 * kT * CPR; idx += 2 * kT) {
-          const int which = idx / (kT * CPR), rem = idx % (kT * CPR);
-          const int row = rem / CPR, c = rem % CPR;
-          if (t.key0 + row < t.Nk) {
-            const uint4 v = *reinterpret_cast<const uint4*>(
-                stage + which * C::TILE + (c / 8) * C::SUB + row * 128 + (((c % 8) ^ (row & 7)) * 16));
-            uint16_t* dst = (which ? a.dk : a.dv) +
-                            ((size_t)t.sv.hk * t.sv.krows + t.sv.k_off + t.key0 + row) * D + c * 8;
-            *reinterpret_cast<uint4*>(dst) = v;
+        // the tiles are written only if every warp staged its part (a warp
+        // whose wait failed has raised the abort flag before arriving; the
+        // flag is read once for the warp, so its lanes leave together)
+        if (!cw_sync(u, 2 + 2 * rd) || !do_epi || __any_sync(0xffffffffu, *abort_flag)) {
+          stop = true;
+          break;
+        }
+        if (!ragged) {
+          if (threadIdx.x == 0) {
+#pragma unroll
+            for (int wl = 0; wl < PER; ++wl)
+#pragma unroll
+              for (int c = 0; c < D / 64; ++c)
+                tma_store_3d((rd * PER + wl) ? &a.tm_dk : &a.tm_dv, stage + wl * C::TILE + c * C::SUB,
+                             c * 64, t.sv.k_off + t.key0, t.sv.hk);
+            bulk_commit_group();
+          }
+        } else {
+          constexpr int CPR = D / 8;   // 16-byte pieces per row
+          for (int idx = threadIdx.x; idx < PER * kT * CPR; idx += 2 * kT) {
+            const int wl = idx / (kT * CPR), rem = idx % (kT * CPR);
+            const int row = rem / CPR, c = rem % CPR;
+            if (t.key0 + row < t.Nk) {
+              const uint4 v = *reinterpret_cast<const uint4*>(
+                  stage + wl * C::TILE + (c / 8) * C::SUB + row * 128 + (((c % 8) ^ (row & 7)) * 16));
+              uint16_t* dst = ((rd * PER + wl) ? a.dk : a.dv) +
+                              ((size_t)t.sv.hk * t.sv.krows + t.sv.k_off + t.key0 + row) * D + c * 8;
+              *reinterpret_cast<uint4*>(dst) = v;
+            }
           }
         }
       }
-      mbar_arrive_warp(&bars.sched_empty[u & 1]);   // done with the slot
+      if (stop) break;
+      mbar_arrive_warp(&bars.sched_empty()[u & 1]);   // done with the slot
     }
-    // reductions and stores complete before the CTA exits
+    // stores complete before the CTA exits
     if (lane == 0) bulk_wait_group0();
     __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::W_MMA) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -872,7 +915,7 @@ cudaError_t launch_main(const BwdBf16Args& a, cudaStream_t s) {
     grid = std::min(n_items, (long)std::max(a.num_sms, 1));
     if ((e = cudaMemsetAsync(a.sched, 0, sizeof(int), s)) != cudaSuccess) return e;
   }
-  kern<<<(unsigned)grid, kThreads, C::BYTES, s>>>(b);
+  kern<<<(unsigned)grid, C::NT, C::BYTES, s>>>(b);
   return cudaGetLastError();
 }
 

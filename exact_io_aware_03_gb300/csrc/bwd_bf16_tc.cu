@@ -49,7 +49,6 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
 constexpr int kT = 128;   // keys per key tile = rows per query tile
 constexpr float kLog2e = 1.4426950408889634f;
 

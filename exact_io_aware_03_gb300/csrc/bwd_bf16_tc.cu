@@ -6,8 +6,9 @@
 //  1. bwd_pre: D_i = rowsum(dO_i o O_i) in fp32, LSE converted to the base-2
 //     domain (a fully masked row's -inf becomes +inf so that its recomputed
 //     probabilities are exactly 0), and the fp32 dQ accumulator zeroed.
-//  2. bwd_main: one CTA per (128-key tile j, head), key/value tile resident in
-//     shared memory; it walks the 128-row query tiles i that can see tile j
+//  2. bwd_main: one work item per (128-key tile j, key/value head), taken by
+//     a persistent CTA (one per SM); the key/value tile stays resident in
+//     shared memory while the item walks the 128-row query tiles i that see j
 //     (causal: only i at or below the bottom-right diagonal) and per tile
 //       S^T  = K_j Q_i^T                      tcgen05 -> TMEM (lane = key)
 //       P^T  = exp2(S^T*c + bias - LSE_i)     recomputed from the saved LSE
@@ -28,11 +29,13 @@
 // order; there is no accumulator to zero and no bwd_post. dO is double-buffered
 // in the shared memory the dS and staging buffers used.
 //
-// Warp roles of bwd_main (320 threads): warps 0-7 are two warpgroups that
+// Warp roles of bwd_main (512 threads): warps 0-7 are two warpgroups that
 // split the query columns of every tile; they compute P^T (kept in fp32
-// registers) and dS^T (thread = key = TMEM lane), read dQ_i out of TMEM
-// (thread = query row) and reduce it into global memory, and write dK/dV at
-// the end; warp 8 issues TMA loads; warp 9 allocates TMEM and issues the MMAs.
+// registers) and dS^T (thread = key = TMEM lane) and write dK/dV at the end
+// of an item; warps 8-11 read dQ_i out of TMEM (thread = query row), stage it
+// in shared memory and reduce-add it into global memory; warp 12 fetches work
+// items and issues TMA loads; warp 13 allocates TMEM and issues the MMAs.
+// The deterministic form has no dQ warps (320 threads: TMA warp 8, MMA 9).
 // TMEM (512 columns): S^T [0,128), then per half h of the query columns the
 // packed bf16 P^T in [64h, 64h+32) (each warpgroup overwrites only scores it
 // has already read); dP^T then dQ [128,256); dV [256,256+D); dK [256+D,256+2D).

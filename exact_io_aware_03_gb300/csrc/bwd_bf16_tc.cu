@@ -493,11 +493,14 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
       {
         // (the whole warp, converged; lane 0 issues each instruction)
         // Issue order per query tile i:  dP(i) [after dQ(i-1) left TMEM],
-        // dV(i) [after P(i)], S(i+1) [the S columns are free once dV(i) has
-        // read P(i)], dQ(i) and dK(i) [after dS(i)]. S(i+1) and the softmax
-        // of tile i+1 thus overlap dQ(i) and dK(i). The first dV and dK of
-        // an item start from zero: the P/dS warps arrive on P of the item's
-        // first tile only after they have read the previous item's dK, dV.
+        // dV(i) [after P(i)], S(i+1) [after Q(i+1) landed; the S columns are
+        // free once dV(i) has read P(i)], dK(i) and dQ(i) [after dS(i)].
+        // S(i+1) and the softmax of tile i+1 thus overlap dK(i) and dQ(i).
+        // dK(i), the last reader of Q(i), goes before dQ(i) so that the load
+        // of Q(i+2) into its stage starts a product earlier. The first dV and
+        // dK of an item start from zero: the P/dS warps arrive on P of the
+        // item's first tile only after they have read the previous item's
+        // dK, dV.
         ok = !__any_sync(0xffffffffu, *abort_flag) && wait_warp(bars.kv_full(), kph & 1, wc, ERR_WAIT_MMA) &&
              wait_warp(&bars.q_full()[g & 1], (g >> 1) & 1, wc, ERR_WAIT_MMA);
         if (ok) {
@@ -511,9 +514,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
           const uint64_t dk16 = opaque(dk16c), dsub = opaque(dsubc);
           // dP^T = V dO^T, once dQ of the previous tile has left TMEM (DET: the
           // dS^T of the previous tile in these columns was read by dK, an
-          // earlier MMA)
-          if (!DET && gi > 0 && !(ok = wait_warp(bars.dq_empty(), (gi - 1) & 1, wc, ERR_WAIT_MMA))) break;
+          // earlier MMA). dO(i) has usually landed long before: its wait
+          // goes first, off the path from dQ(i-1) to dP(i).
           if (!(ok = wait_warp(&bars.do_full()[sd], (gi / C::ND) & 1, wc, ERR_WAIT_MMA))) break;
+          if (!DET && gi > 0 && !(ok = wait_warp(bars.dq_empty(), (gi - 1) & 1, wc, ERR_WAIT_MMA))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -521,12 +525,9 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
             mma_ss_w(t_dp, sdesc_offset(dk16, C::OFF_V + o), sdesc_offset(dk16, do_o + o), id_s, kk > 0);
           }
           mma_commit_w(bars.dp_full());
-          // dV(i) and S(i+1) are issued back to back once both can go: a wait
-          // between two products would let the MMA queue run dry
+          // dV(i) as soon as P(i) is in TMEM; the wait for Q(i+1), which
+          // often lands later than P(i), then runs while dV(i) computes
           if (!(ok = wait_warp(bars.p_full(), gi & 1, wc, ERR_WAIT_MMA))) break;
-          if (lt + 1 < n &&
-              !(ok = wait_warp(&bars.q_full()[(gi + 1) & 1], ((gi + 1) >> 1) & 1, wc, ERR_WAIT_MMA)))
-            break;
           tc_fence_after();
           // dV += P^T dO  (P^T packed bf16: query columns [0,64) in TMEM columns
           // [0,32), [64,128) in [64,96))
@@ -535,7 +536,11 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
             mma_ts_w(t_dv, t_s + (kk / 4) * 64 + (kk % 4) * 8, sdesc_offset(dsub, do_o + kk * 2048), id_acc,
                    (lt > 0 || kk > 0) ? 1u : 0u);
           mma_commit_w(&bars.do_empty()[sd]);   // dV is the last reader of dO(i)
-          if (lt + 1 < n) issue_s(gi + 1);
+          if (lt + 1 < n) {
+            if (!(ok = wait_warp(&bars.q_full()[(gi + 1) & 1], ((gi + 1) >> 1) & 1, wc, ERR_WAIT_MMA))) break;
+            tc_fence_after();
+            issue_s(gi + 1);
+          }
           if (!(ok = wait_warp(bars.ds_full(), gi & 1, wc, ERR_WAIT_MMA))) break;
           tc_fence_after();
           if constexpr (DET) {
@@ -546,19 +551,18 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
                      id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
             mma_commit_w(&bars.q_empty()[s]);
           } else {
-            // dQ = dS K, then dK += dS^T Q (A = dS^T: K-major view of the dS
-            // boxes): dQ first, so that its read-out (which gates the next
-            // dP) starts a product earlier
-#pragma unroll
-            for (int kk = 0; kk < kT / 16; ++kk)
-              mma_ss_w(t_dp, sdesc_offset(dsub, C::OFF_DS + kk * 2048),
-                     sdesc_offset(dsub, C::OFF_K + kk * 2048), id_dq, kk > 0 ? 1u : 0u);
-            mma_commit_w(bars.dq_full());
+            // dK += dS^T Q (A = dS^T: K-major view of the dS boxes), which
+            // frees the Q stage, then dQ = dS K
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
               mma_ss_w(t_dk, sdesc_offset(dk16, C::OFF_DS + (kk / 4) * C::SUB + (kk % 4) * 32),
                      sdesc_offset(dsub, q_o + kk * 2048), id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
             mma_commit_w(&bars.q_empty()[s]);
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_ss_w(t_dp, sdesc_offset(dsub, C::OFF_DS + kk * 2048),
+                     sdesc_offset(dsub, C::OFF_K + kk * 2048), id_dq, kk > 0 ? 1u : 0u);
+            mma_commit_w(bars.dq_full());
           }
         }
         // every MMA of this item: its K/V buffers are free, dK and dV final
@@ -665,15 +669,17 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
       const float kb =
           key < cur->nk ? (BIAS ? a.bias[(size_t)cur->bias_row + key] * kLog2e : 0.f) : -INFINITY;
       const int thr = key - off - q0 - h * 64;   // local column < thr -> masked
+      // the second 32 scores load while the first 32 are exponentiated
       uint32_t* sv = reinterpret_cast<uint32_t*>(P);
       tmem_ld32(lane_base + h * 64, sv);
-      tmem_ld32(lane_base + h * 64 + 32, sv + 32);
       tmem_ld_wait();
+      tmem_ld32(lane_base + h * 64 + 32, sv + 32);
       const uint64_t sl2x2 = f2_pack(sl2, sl2), kb2 = f2_pack(kb, kb);
       // x = S * scale * log2(e) + key bias - LSE * log2(e) (the key term is
       // -inf for a key past the end of a ragged tile)
 #pragma unroll
       for (int e = 0; e < 64; e += 4) {
+        if (e == 32) tmem_ld_wait_regs32(sv + 32);
         const float4 L4 = *reinterpret_cast<const float4*>(stl + e);   // -LSE * log2(e)
         float x[4];
         f2_unpack(add2(fma2(f2_pack(P[e], P[e + 1]), sl2x2, kb2), f2_pack(L4.x, L4.y)), x[0], x[1]);

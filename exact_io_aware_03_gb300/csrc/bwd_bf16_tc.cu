@@ -178,7 +178,12 @@ struct BwdCfg {
   // per Q stage: base-2 LSE [128] then D [128] of the tile's rows (TMA)
   static constexpr int OFF_STAT = OFF_DS + (DET ? 0 : kT * kT * 2);
   static constexpr int OFF_BAR = OFF_STAT + 2 * 2 * kT * 4;
-  static constexpr int NBAR = 18 + 2 * ND;   // see BwdBars
+  static constexpr int NBAR = 20 + 2 * ND;   // see BwdBars
+  // dK/dV write-out of an item: both tiles staged at once, dV in the dS
+  // buffer and (reduction form, d = 128) dK in the Q stage of the item's last
+  // tile, which the item no longer reads; at d = 64 both fit the dS buffer;
+  // the deterministic form stages them in the Q stages (one item per CTA)
+  static constexpr bool DK_IN_Q = !DET && 2 * TILE > 32768;
   static constexpr int OFF_SCALARS = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_SCALARS + 16 + 2 * 48;   // flags, then the work-item ring
 };
@@ -214,6 +219,11 @@ struct BwdBars {
   __device__ __forceinline__ uint64_t* sched_empty() const { return b + 15 + 2 * ND; }
   // barrier of the P/dS warps (one arrival per warp)
   __device__ __forceinline__ uint64_t* cw() const { return b + 17 + 2 * ND; }
+  // reduction form, once per item: its dK/dV staged by the P/dS warps (one
+  // arrival per warp); the staging read by the TMA stores (one arrival, from
+  // the TMA warp)
+  __device__ __forceinline__ uint64_t* epi_staged() const { return b + 18 + 2 * ND; }
+  __device__ __forceinline__ uint64_t* epi_read() const { return b + 19 + 2 * ND; }
 };
 
 
@@ -338,6 +348,8 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
     mbar_init(bars.dq_empty(), 4);            // one arrival per dQ warp
     mbar_init(bars.drain(), 1);
     mbar_init(bars.cw(), 2 * kT / 32);
+    mbar_init(bars.epi_staged(), 2 * kT / 32);
+    mbar_init(bars.epi_read(), 1);
     *abort_flag = (smem_u32(smem) & 1023u) != 0;
     fence_mbar_init();
   }
@@ -363,6 +375,11 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
     int g = 0, kph = 0;     // query-tile steps / non-empty items so far
     int nq = 0, nd = 0, nkv = 0;   // Q / dO / K,V fills issued
     bool ok = true;
+    // the previous item's dK/dV stores (reduction form): ragged tile (written
+    // by the P/dS warps themselves), first key row, key/value head, Q stage
+    // holding dK
+    bool pv_ragged = false;
+    int pv_row = 0, pv_hk = 0, pv_sk = 0;
     for (int u = 0; ok; ++u) {
       int w;
       if (DET) {
@@ -401,47 +418,85 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok || w < 0) break;
-      if (n == 0) continue;
-      if (lane == 0 && !*abort_flag) {
-        // K and V of the previous item are free once all of its MMAs are done
-        if (kph > 0 && !wait1(bars.kv_empty(), (kph - 1) & 1, wc, ERR_WAIT_LOAD)) ok = false;
-        if (ok) {
-          mbar_arrive_expect_tx(bars.kv_full(), 2 * C::TILE);
+      if (!ok) break;
+      // step lt's Q (with its statistics) and dO
+      auto load_step = [&](int lt) -> bool {
+        const int gi = g + lt, s = gi & 1, uq = gi >> 1;
+        const int q0 = q_row0(t, lt), hq = q_head(t, lt);
+        if (uq > 0 && !wait1(&bars.q_empty()[s], (uq - 1) & 1, wc, ERR_WAIT_LOAD)) return false;
+        mbar_arrive_expect_tx(&bars.q_full()[s], C::TILE + 2 * kT * 4);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * C::SUB, &a.tm_q, c * 64, t.sv.q_off + q0,
+                      q_coord(t, hq), &bars.q_full()[s]);
+        float* st = reinterpret_cast<float*>(smem + C::OFF_STAT) + s * 2 * kT;
+        const size_t srow = ((size_t)t.b * p.H + hq) * a.nq_pad + q0;
+        bulk_load_1d(st, a.lse2 + srow, kT * 4, &bars.q_full()[s]);
+        bulk_load_1d(st + kT, a.D + srow, kT * 4, &bars.q_full()[s]);
+        ++nq;
+        // dO stage sd may be refilled once dV of its previous tile is done
+        const int sd = gi % C::ND, ud = gi / C::ND;
+        if (ud > 0 && !wait1(&bars.do_empty()[sd], (ud - 1) & 1, wc, ERR_WAIT_LOAD)) return false;
+        mbar_arrive_expect_tx(&bars.do_full()[sd], C::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::OFF_DO + sd * C::TILE + c * C::SUB, &a.tm_do, c * 64, t.sv.q_off + q0,
+                      q_coord(t, hq), &bars.do_full()[sd]);
+        ++nd;
+        return true;
+      };
+      // Reduction form: the TMA stores of the previous item's dK and dV, once
+      // the P/dS warps have staged them; then the staging buffers are handed
+      // back (the dS buffer to the P/dS warps, the Q stage that held dK to
+      // the loads below: it is refilled at the second tile of this item at
+      // the earliest, so every load into it follows this).
+      auto store_prev = [&]() -> bool {
+        if (!wait1(bars.epi_staged(), (u - 1) & 1, wc, ERR_WAIT_LOAD)) return false;
+        if (!pv_ragged) {
+          uint8_t* st_dk = C::DK_IN_Q ? smem + C::OFF_Q + pv_sk * C::TILE : smem + C::OFF_DS + C::TILE;
           for (int c = 0; c < D / 64; ++c) {
-            tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, t.sv.k_off + t.key0, t.sv.hk,
-                        bars.kv_full());
-            tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, t.sv.k_off + t.key0, t.sv.hk,
-                        bars.kv_full());
+            tma_store_3d(&a.tm_dv, smem + C::OFF_DS + c * C::SUB, c * 64, pv_row, pv_hk);
+            tma_store_3d(&a.tm_dk, st_dk + c * C::SUB, c * 64, pv_row, pv_hk);
           }
-          ++nkv;
+          bulk_commit_group();
+          bulk_wait_group_read0();
         }
-        for (int lt = 0; lt < n && ok; ++lt) {
-          const int gi = g + lt, s = gi & 1, uq = gi >> 1;
-          const int q0 = q_row0(t, lt), hq = q_head(t, lt);
-          if (uq > 0 && !wait1(&bars.q_empty()[s], (uq - 1) & 1, wc, ERR_WAIT_LOAD)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars.q_full()[s], C::TILE + 2 * kT * 4);
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * C::SUB, &a.tm_q, c * 64,
-                        t.sv.q_off + q0, q_coord(t, hq), &bars.q_full()[s]);
-          float* st = reinterpret_cast<float*>(smem + C::OFF_STAT) + s * 2 * kT;
-          const size_t srow = ((size_t)t.b * p.H + hq) * a.nq_pad + q0;
-          bulk_load_1d(st, a.lse2 + srow, kT * 4, &bars.q_full()[s]);
-          bulk_load_1d(st + kT, a.D + srow, kT * 4, &bars.q_full()[s]);
-          ++nq;
-          // dO stage sd may be refilled once dV of its previous tile is done
-          const int sd = gi % C::ND, ud = gi / C::ND;
-          if (ud > 0 && !wait1(&bars.do_empty()[sd], (ud - 1) & 1, wc, ERR_WAIT_LOAD)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars.do_full()[sd], C::TILE);
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + C::OFF_DO + sd * C::TILE + c * C::SUB, &a.tm_do, c * 64,
-                        t.sv.q_off + q0, q_coord(t, hq), &bars.do_full()[sd]);
-          ++nd;
+        mbar_arrive(bars.epi_read());
+        return true;
+      };
+      if (w < 0) {
+        if (!DET && u > 0 && lane == 0 && !*abort_flag) store_prev();
+        break;
+      }
+      if (lane == 0 && !*abort_flag) {
+        // the first tile's Q and dO go out before K and V, which wait for
+        // the previous item's last product
+        if (n > 0) ok = load_step(0);
+        if (n > 0 && ok) {
+          // K and V of the previous item are free once all of its MMAs are done
+          if (kph > 0 && !wait1(bars.kv_empty(), (kph - 1) & 1, wc, ERR_WAIT_LOAD)) ok = false;
+          if (ok) {
+            mbar_arrive_expect_tx(bars.kv_full(), 2 * C::TILE);
+            for (int c = 0; c < D / 64; ++c) {
+              tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * 64, t.sv.k_off + t.key0, t.sv.hk,
+                          bars.kv_full());
+              tma_load_3d(smem + C::OFF_V + c * C::SUB, &a.tm_v, c * 64, t.sv.k_off + t.key0, t.sv.hk,
+                          bars.kv_full());
+            }
+            ++nkv;
+          }
         }
+        if (!DET && u > 0 && ok) ok = store_prev();
+        for (int lt = 1; lt < n && ok; ++lt) ok = load_step(lt);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      if constexpr (!DET) {
+        // where this item's dK/dV go and where dK is staged
+        pv_ragged = p.cu_k != nullptr && t.key0 + kT > t.Nk;
+        pv_row = t.sv.k_off + t.key0;
+        pv_hk = t.sv.hk;
+        pv_sk = (g + n + 1) & 1;   // the Q stage of the item's last tile
+      }
       g += n;
-      ++kph;
+      if (n > 0) ++kph;
     }
     if (lane == 0) {
       // Drain: wait (bounded, ignoring the abort flag) for the last fill of
@@ -451,6 +506,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
       for (int i = max(0, nq - 2); i < nq; ++i) wait1(&bars.q_full()[i & 1], (i >> 1) & 1, wd, ERR_WAIT_DRAIN);
       for (int i = max(0, nd - C::ND); i < nd; ++i)
         wait1(&bars.do_full()[i % C::ND], (i / C::ND) & 1, wd, ERR_WAIT_DRAIN);
+      if (!DET) bulk_wait_group0();   // the dK/dV stores are complete
     }
   } else if (warp == C::W_MMA) {
     // ================================================================ MMA issuer
@@ -760,21 +816,22 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
       return true;
     };
 
-    // The staging of dK and dV: the Q stages in the deterministic form (one
-    // item per CTA: free once its MMAs are done); otherwise the dS buffer,
-    // in two rounds (dV, then dK) at d = 128, whose next writers wait until
-    // TMA has read the staging, so the next item's loads are not held up.
-    uint8_t* stage = DET ? smem + C::OFF_Q : smem + C::OFF_DS;   // [D/64 boxes][128 keys][128 B] per tensor
-    constexpr int ROUNDS = (!DET && 2 * C::TILE > 32768) ? 2 : 1;
-    constexpr int PER = 2 / ROUNDS;   // tensors staged per round
-    // barrier of the eight compute warps, on an mbarrier so that a warp that
-    // has stopped makes the others' wait run out instead of hang. Item u
-    // uses it 1 + 2 * ROUNDS times (the first use, j = 0, only for u > 0);
-    // use j of item u is phase U u - 1 + j.
-    constexpr int U = 1 + 2 * ROUNDS;
-    auto cw_sync = [&](int u, int j) -> bool {
+    // The staging of dK and dV, one tile each, as the 128-byte-swizzled
+    // 64-column boxes TMA uses. Deterministic form (one item per CTA): in the
+    // Q stages, stored by one of these threads. Reduction form: dV in the dS
+    // buffer and dK in the Q stage of the item's last tile (d = 64: both in
+    // the dS buffer), stored by the TMA warp, which hands the dS buffer back
+    // once TMA has read it (epi_read) and refills that Q stage only after
+    // the read; so the write-out costs the P/dS warps one pass, and the next
+    // item's loads and first products go on meanwhile.
+    // Barrier of the eight compute warps, on an mbarrier so that a warp that
+    // has stopped makes the others' wait run out instead of hang.
+    // Used once per ragged item in the reduction form, once in the
+    // deterministic form (one item per CTA).
+    int ncw = 0;   // uses so far (the same count in every compute warp)
+    auto cw_sync = [&]() -> bool {
       mbar_arrive_warp(bars.cw());
-      return wait_warp(bars.cw(), (U * u - 1 + j) & 1, wc, ERR_WAIT_EPILOGUE);
+      return wait_warp(bars.cw(), DET ? 0u : (uint32_t)(ncw++ & 1), wc, ERR_WAIT_EPILOGUE);
     };
     for (int u = 0;; ++u) {
       if (!wait_warp(&bars.sched_full()[u & 1], (u >> 1) & 1, wc, ERR_WAIT_LOAD)) break;
@@ -788,13 +845,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
       int lt = 0;
       const int g = cur->g0;
       if (n > 0) ok = compute_p(g);
-      if (u > 0) {
-        // every compute warp passes here once per item, even after a failed
-        // wait: the previous item's dK/dV staging has been read by TMA
-        // before anything writes it again
-        if (!DET && threadIdx.x == 0) bulk_wait_group_read0();
-        if (!cw_sync(u, 0)) ok = false;
-      }
+      // the previous item's staging has been read by TMA before the dS buffer
+      // is written again (every compute warp waits once per item, even after
+      // a failed wait, so that the phases stay in step)
+      if (!DET && u > 0 && !wait_warp(bars.epi_read(), (u - 1) & 1, wc, ERR_WAIT_EPILOGUE)) ok = false;
       if (n > 0) {
         for (; ok && lt < n; ++lt) {
           const int gi = g + lt;
@@ -802,85 +856,81 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
           if (lt + 1 < n && !(ok = compute_p(gi + 1))) break;
         }
         if (ok) {
-          // every MMA of the item is done (the last dK follows the last dQ)
+          // every MMA of the item is done (the last dQ follows the last dK)
           ok = wait_warp(bars.kv_empty(), cur->kph & 1, wc, ERR_WAIT_EPILOGUE);
           tc_fence_after();
         }
       }
       // ---- dK, dV of this key tile. Each thread reads its key row (this
-      // warpgroup's half of the columns) out of TMEM and stages it in shared
-      // memory as the 128-byte-swizzled 64-column boxes TMA uses; one thread
-      // then stores the tiles with TMA. A packed sequence's ragged last tile
-      // is written with plain coalesced stores instead (a 128-row box would
-      // run into the next sequence's rows). Every compute warp reaches each
-      // barrier once per item.
+      // warpgroup's half of the columns) out of TMEM and stages it. A packed
+      // sequence's ragged last tile is written with plain coalesced stores
+      // instead of TMA (a 128-row box would run into the next sequence's
+      // rows).
       const BwdItem t = bwd_item<CAUSAL>(a, cur->w);
       const bool ragged = p.cu_k != nullptr && t.key0 + kT > t.Nk;
-      bool stop = false;
+      uint8_t* stg[2];   // staging of dV, dK
+      if (DET) {
+        stg[0] = smem + C::OFF_Q;
+        stg[1] = smem + C::OFF_Q + C::TILE;
+      } else {
+        stg[0] = smem + C::OFF_DS;
+        stg[1] = C::DK_IN_Q ? smem + C::OFF_Q + ((g + n + 1) & 1) * C::TILE : smem + C::OFF_DS + C::TILE;
+      }
+      if (ok) {
+        const bool have = n > 0;
 #pragma unroll
-      for (int rd = 0; rd < ROUNDS; ++rd) {
-        // the staging is free: the item's MMAs are done (each warp waited)
-        // and the previous round's (or item's) staging has been read
-        if (rd > 0 && threadIdx.x == 0) bulk_wait_group_read0();
-        if (!cw_sync(u, 1 + 2 * rd)) ok = false;
-        const bool do_epi = ok;
-        if (do_epi) {
-          const bool have = n > 0;
+        for (int which = 0; which < 2; ++which) {   // 0: dV, 1: dK
 #pragma unroll
-          for (int wl = 0; wl < PER; ++wl) {
-            const int which = rd * PER + wl;   // 0: dV, 1: dK
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            uint32_t x[32];
+            if (have) {
+              tmem_ld32(lane_base + 256 + which * D + h * HD + c0, x);
+              tmem_ld_wait();
+            } else {
 #pragma unroll
-            for (int c0 = 0; c0 < HD; c0 += 32) {
-              uint32_t x[32];
-              if (have) {
-                tmem_ld32(lane_base + 256 + which * D + h * HD + c0, x);
-                tmem_ld_wait();
-              } else {
+              for (int e = 0; e < 32; ++e) x[e] = 0u;
+            }
+            uint32_t pkd[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] = 0u;
-              }
-              uint32_t pkd[16];
+            for (int e = 0; e < 32; e += 2)
+              pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+            const int col = h * HD + c0;   // first column of these 32
+            uint8_t* rowp = stg[which] + (col / 64) * C::SUB + r * 128;
 #pragma unroll
-              for (int e = 0; e < 32; e += 2)
-                pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
-              const int col = h * HD + c0;   // first column of these 32
-              uint8_t* rowp = stage + wl * C::TILE + (col / 64) * C::SUB + r * 128;
-#pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4) {
-                const int j = (col % 64) / 8 + v4;
-                *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) * 16)) =
-                    make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
-              }
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const int j = (col % 64) / 8 + v4;
+              *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) * 16)) =
+                  make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
             }
           }
-          fence_proxy_async_smem();   // the generic-proxy writes, before TMA reads them
         }
-        // the tiles are written only if every warp staged its part (a warp
-        // whose wait failed has raised the abort flag before arriving; the
-        // flag is read once for the warp, so its lanes leave together)
-        if (!cw_sync(u, 2 + 2 * rd) || !do_epi || __any_sync(0xffffffffu, *abort_flag)) {
-          stop = true;
-          break;
-        }
-        if (!ragged) {
+        fence_proxy_async_smem();   // the generic-proxy writes, before TMA reads them
+      }
+      // (the abort flag is read once for the warp, so its lanes leave together)
+      bool stop = !ok || __any_sync(0xffffffffu, *abort_flag);
+      if (DET || ragged) {
+        // every warp's rows staged; a warp whose wait failed has raised the
+        // abort flag before arriving
+        if (!cw_sync() || __any_sync(0xffffffffu, *abort_flag)) stop = true;
+        if (!stop && !ragged) {
           if (threadIdx.x == 0) {
 #pragma unroll
-            for (int wl = 0; wl < PER; ++wl)
+            for (int which = 0; which < 2; ++which)
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
-                tma_store_3d((rd * PER + wl) ? &a.tm_dk : &a.tm_dv, stage + wl * C::TILE + c * C::SUB,
-                             c * 64, t.sv.k_off + t.key0, t.sv.hk);
+                tma_store_3d(which ? &a.tm_dk : &a.tm_dv, stg[which] + c * C::SUB, c * 64,
+                             t.sv.k_off + t.key0, t.sv.hk);
             bulk_commit_group();
           }
-        } else {
+        } else if (!stop) {
           constexpr int CPR = D / 8;   // 16-byte pieces per row
-          for (int idx = threadIdx.x; idx < PER * kT * CPR; idx += 2 * kT) {
-            const int wl = idx / (kT * CPR), rem = idx % (kT * CPR);
+          for (int idx = threadIdx.x; idx < 2 * kT * CPR; idx += 2 * kT) {
+            const int which = idx / (kT * CPR), rem = idx % (kT * CPR);
             const int row = rem / CPR, c = rem % CPR;
             if (t.key0 + row < t.Nk) {
               const uint4 v = *reinterpret_cast<const uint4*>(
-                  stage + wl * C::TILE + (c / 8) * C::SUB + row * 128 + (((c % 8) ^ (row & 7)) * 16));
-              uint16_t* dst = ((rd * PER + wl) ? a.dk : a.dv) +
+                  stg[which] + (c / 8) * C::SUB + row * 128 + (((c % 8) ^ (row & 7)) * 16));
+              uint16_t* dst = (which ? a.dk : a.dv) +
                               ((size_t)t.sv.hk * t.sv.krows + t.sv.k_off + t.key0 + row) * D + c * 8;
               *reinterpret_cast<uint4*>(dst) = v;
             }
@@ -888,10 +938,12 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
         }
       }
       if (stop) break;
+      // reduction form: staged (a ragged tile: already stored) -> the TMA warp
+      if (!DET) mbar_arrive_warp(bars.epi_staged());
       mbar_arrive_warp(&bars.sched_empty()[u & 1]);   // done with the slot
     }
-    // stores complete before the CTA exits
-    if (lane == 0) bulk_wait_group0();
+    // (deterministic form) the stores are complete before the CTA exits
+    if (DET && lane == 0) bulk_wait_group0();
     __syncwarp();
   }
 

@@ -63,6 +63,11 @@ def make(B, H, Nq, Nk, d, seed=0, bias=None):
     elif bias == "all_masked_first_batch":
         b = torch.randn(B, Nk, generator=g)
         b[0] = -math.inf
+    elif bias == "pad_mixed":
+        # even batches keep their first 300 keys, odd ones all: runs of key
+        # tiles with nothing to compute next to full ones
+        b = torch.zeros(B, Nk)
+        b[0::2, 300:] = -math.inf
     return q, k, v, dO, b
 
 
@@ -82,6 +87,11 @@ SMALL = [
     (3, 1, 257, 1, 128, False, None),
     (1, 1, 64, 2048, 128, False, None),       # many key tiles: many dQ reductions per row
     (1, 1, 2048, 64, 128, False, None),       # many query tiles per key tile
+    # more key tiles than SMs: several per persistent CTA, with runs of
+    # fully masked ones between full ones (the dK/dV write-out hand-over)
+    (2, 8, 256, 2048, 128, False, "pad_mixed"),
+    (2, 8, 256, 2048, 64, True, "pad_mixed"),
+    (1, 12, 384, 2048, 128, True, None),
 ]
 
 

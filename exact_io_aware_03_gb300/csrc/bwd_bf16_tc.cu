@@ -868,14 +868,13 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
       // rows).
       const BwdItem t = bwd_item<CAUSAL>(a, cur->w);
       const bool ragged = p.cu_k != nullptr && t.key0 + kT > t.Nk;
-      uint8_t* stg[2];   // staging of dV, dK
-      if (DET) {
-        stg[0] = smem + C::OFF_Q;
-        stg[1] = smem + C::OFF_Q + C::TILE;
-      } else {
-        stg[0] = smem + C::OFF_DS;
-        stg[1] = C::DK_IN_Q ? smem + C::OFF_Q + ((g + n + 1) & 1) * C::TILE : smem + C::OFF_DS + C::TILE;
-      }
+      // staging of dV (which = 0) and dK (which = 1)
+      const int sk = (g + n + 1) & 1;
+      auto stg = [&](int which) -> uint8_t* {
+        if (DET) return smem + C::OFF_Q + which * C::TILE;
+        if (which == 0) return smem + C::OFF_DS;
+        return C::DK_IN_Q ? smem + C::OFF_Q + sk * C::TILE : smem + C::OFF_DS + C::TILE;
+      };
       if (ok) {
         const bool have = n > 0;
 #pragma unroll
@@ -895,7 +894,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
             for (int e = 0; e < 32; e += 2)
               pkd[e / 2] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
             const int col = h * HD + c0;   // first column of these 32
-            uint8_t* rowp = stg[which] + (col / 64) * C::SUB + r * 128;
+            uint8_t* rowp = stg(which) + (col / 64) * C::SUB + r * 128;
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
               const int j = (col % 64) / 8 + v4;
@@ -918,7 +917,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
             for (int which = 0; which < 2; ++which)
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
-                tma_store_3d(which ? &a.tm_dk : &a.tm_dv, stg[which] + c * C::SUB, c * 64,
+                tma_store_3d(which ? &a.tm_dk : &a.tm_dv, stg(which) + c * C::SUB, c * 64,
                              t.sv.k_off + t.key0, t.sv.hk);
             bulk_commit_group();
           }
@@ -929,7 +928,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
             const int row = rem / CPR, c = rem % CPR;
             if (t.key0 + row < t.Nk) {
               const uint4 v = *reinterpret_cast<const uint4*>(
-                  stg[which] + (c / 8) * C::SUB + row * 128 + (((c % 8) ^ (row & 7)) * 16));
+                  stg(which) + (c / 8) * C::SUB + row * 128 + (((c % 8) ^ (row & 7)) * 16));
               uint16_t* dst = (which ? a.dk : a.dv) +
                               ((size_t)t.sv.hk * t.sv.krows + t.sv.k_off + t.key0 + row) * D + c * 8;
               *reinterpret_cast<uint4*>(dst) = v;

@@ -317,7 +317,6 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
 
-  uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   const BwdBars<C::ND> bars{reinterpret_cast<uint64_t*>(smem + C::OFF_BAR)};
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_SCALARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SCALARS + 4);

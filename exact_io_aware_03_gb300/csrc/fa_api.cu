@@ -5,7 +5,6 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
-#include <cstring>
 #include <mutex>
 
 #include <cuda.h>
@@ -179,7 +178,7 @@ fa_status check_varlen(int total_q, int total_k, int max_q, int max_k, int d, co
 // Tensor maps and pointers of the bf16 forward (everything but the split).
 fa_status fwd_bf16_setup(fa::FwdBf16Args* a, const fa::Problem& p, const void* q, const void* k,
                          const void* v, const float* key_bias, void* o, float* lse) {
-  std::memset(a, 0, sizeof(*a));
+  *a = fa::FwdBf16Args{};
   a->p = p;
   const int BH = p.B * p.H;
   fa_status st;
@@ -255,8 +254,7 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
   p.cu_k = cu_seqlens_k;
   p.total_q = total_q;
   p.total_k = total_k;
-  fa::FwdBf16Args a;
-  std::memset(&a, 0, sizeof(a));
+  fa::FwdBf16Args a{};
   a.p = p;
   if ((st = make_map(&a.tm_q, q, H, total_q, d)) != FA_OK) return st;
   if ((st = make_map(&a.tm_k, k, H_kv, total_k, d)) != FA_OK) return st;
@@ -361,8 +359,7 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   const size_t dq_rows = det ? 0 : varlen ? (size_t)H * total_q : (size_t)B * H * Nq;
   if (workspace_bytes < bwd_ws_bytes(B, H, Nq, dq_rows, d)) return FA_ERR_INVALID_ARG;
 
-  fa::BwdBf16Args a;
-  std::memset(&a, 0, sizeof(a));
+  fa::BwdBf16Args a{};
   a.p = fa::Problem{B, H, Nq, Nk, d, scale, causal ? 1 : 0, Hkv};
   a.p.cu_q = cu_q;
   a.p.cu_k = cu_k;
@@ -553,8 +550,7 @@ fa_status fa_fwd_fp8_stage(const void* q, const void* k, const void* v, const fl
     if (fa::launch_quant_fp8(qa, s) != cudaSuccess) return FA_ERR_CUDA;
   }
   if (stage == 0 || stage == 2) {
-    fa::FwdBf16Args a;
-    std::memset(&a, 0, sizeof(a));
+    fa::FwdBf16Args a{};
     a.p = fa::Problem{B, H, Nq, Nk, d, scale, causal ? 1 : 0, H_kv};
     if ((st = make_map_u8(&a.tm_q, ws + w.q8, d, Nq, (long)B * H)) != FA_OK) return st;
     if ((st = make_map_u8(&a.tm_k, ws + w.k8, d, Nk, (long)B * H_kv)) != FA_OK) return st;

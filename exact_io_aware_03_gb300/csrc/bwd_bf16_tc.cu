@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
         tc_fence_after();
         uint32_t x[D];
 #pragma unroll
-        for (int c = 0; c < D; c += 32) tmem_ld32(lane_base + 128 + c, x + c);
+        for (int c = 0; c < D; c += 64) tmem_ld64(lane_base + 128 + c, x + c);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive_warp(bars.dq_empty());

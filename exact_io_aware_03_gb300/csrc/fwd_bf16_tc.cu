@@ -157,8 +157,69 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
   const int q_base = pair * 2 * kBM;
   const float* bias_row = BIAS ? a.bias + (size_t)b * Nk : nullptr;
 
-  // ---- set-up: barriers, TMEM, optional scan of the bias row
-  if (threadIdx.x == 0) {
+  // ---- key-tile ranges [lo, hi_t) of the two query tiles, from the keys
+  // [klo, khi] that can be visible: the whole sequence, or (with a bias) the
+  // first to the last key with a finite bias, known after the scan below
+  const int n_kv = (Nk + kBN - 1) / kBN;
+  int lo = 0, hi = 0;
+  int hi_t[2] = {0, 0};
+  bool any = false;
+  auto set_ranges = [&](int klo, int khi) {
+    int hi_all;
+    if (khi < 0) {
+      lo = hi_all = 0;
+    } else {
+      lo = klo / kBN;
+      hi_all = khi / kBN + 1;
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int r0 = q_base + t * kBM;
+      int h = hi_all;
+      if (r0 >= Nq) {
+        h = lo;   // tile past the last query row: inactive
+      } else if (CAUSAL) {
+        const long last_row = min(r0 + kBM - 1, Nq - 1);
+        const long lim = last_row + (long)Nk - Nq;
+        h = lim < 0 ? 0 : (int)min((long)hi_all, lim / kBN + 1);
+      }
+      hi_t[t] = max(h, lo);
+    }
+    if (a.n_split > 1) {
+      // split-KV: this CTA covers key tiles [s_lo, s_hi) of its query tiles only
+      const int per = (n_kv + a.n_split - 1) / a.n_split;
+      const int s_lo = (int)blockIdx.y * per, s_hi = min(n_kv, s_lo + per);
+      lo = max(lo, s_lo);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) hi_t[t] = max(lo, min(hi_t[t], s_hi));
+    }
+    hi = max(hi_t[0], hi_t[1]);
+    any = hi > lo;
+  };
+  if (!BIAS) set_ranges(0, Nk - 1);
+  // the producer thread's first loads, in the order the first products use
+  // them: Q of tile 0, K of the first key tile, Q of tile 1
+  auto first_loads = [&]() {
+    for (int t = 0; t < 2; ++t) {
+      if (hi_t[t] > lo) {
+        mbar_arrive_expect_tx(&bars.q_full[t], C::TILE);
+        for (int c = 0; c < C::NBOX; ++c)
+          tma_load_3d(smem + C::OFF_Q + t * C::TILE + c * C::SUB, &a.tm_q, c * (128 / C::EB),
+                      sv.q_off + q_base + t * kBM, sv.hq, &bars.q_full[t]);
+      }
+      if (t == 0) {
+        mbar_arrive_expect_tx(bars.k0_full, C::TILE);
+        for (int c = 0; c < C::NBOX; ++c)
+          tma_load_3d(smem + C::OFF_K + c * C::SUB, &a.tm_k, c * (128 / C::EB), sv.k_off + lo * kBN,
+                      sv.hk, bars.k0_full);
+      }
+    }
+  };
+
+  // ---- set-up: barriers, TMEM, optional scan of the bias row. Without a
+  // bias the producer thread issues the first loads right after initialising
+  // the barriers, under the rest of the set-up.
+  if (warp == 8 && lane == 0) {
     mbar_init(&bars.q_full[0], 1);
     mbar_init(&bars.q_full[1], 1);
     for (int s = 0; s < C::NS; ++s) {
@@ -180,82 +241,39 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
     if (sv.bad && pair == n_pairs - 1) atomicOr(a.err, ERR_BAD_SEQLEN);
     *key_hi_s = -1;
     fence_mbar_init();
+    tma_prefetch_desc(&a.tm_q);
+    tma_prefetch_desc(&a.tm_k);
+    tma_prefetch_desc(&a.tm_v);
+    if (!BIAS && any) first_loads();
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
-    tma_prefetch_desc(&a.tm_q);
-    tma_prefetch_desc(&a.tm_k);
-    tma_prefetch_desc(&a.tm_v);
-  }
   __syncthreads();
   if (BIAS) {
     // first and last key with a finite bias; tiles outside are skipped
-    int lo = Nk, hi = -1;
+    int klo = Nk, khi = -1;
     for (int j = threadIdx.x; j < Nk; j += kThreads) {
       if (bias_row[j] != -INFINITY) {
-        lo = min(lo, j);
-        hi = max(hi, j);
+        klo = min(klo, j);
+        khi = max(khi, j);
       }
     }
-    if (lo < Nk) atomicMin(key_lo_s, lo);
-    if (hi >= 0) atomicMax(key_hi_s, hi);
+    if (klo < Nk) atomicMin(key_lo_s, klo);
+    if (khi >= 0) atomicMax(key_hi_s, khi);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // ---- key-tile ranges [lo, hi_t) of the two query tiles
-  const int n_kv = (Nk + kBN - 1) / kBN;
-  int lo = 0, hi_all = n_kv;
-  if (BIAS) {
-    const int klo = *key_lo_s, khi = *key_hi_s;
-    if (khi < 0) {
-      lo = hi_all = 0;
-    } else {
-      lo = klo / kBN;
-      hi_all = khi / kBN + 1;
-    }
-  }
-  int hi_t[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int r0 = q_base + t * kBM;
-    int h = hi_all;
-    if (r0 >= Nq) {
-      h = lo;   // tile past the last query row: inactive
-    } else if (CAUSAL) {
-      const long last_row = min(r0 + kBM - 1, Nq - 1);
-      const long lim = last_row + (long)Nk - Nq;
-      h = lim < 0 ? 0 : (int)min((long)hi_all, lim / kBN + 1);
-    }
-    hi_t[t] = max(h, lo);
-  }
-  if (a.n_split > 1) {
-    // split-KV: this CTA covers key tiles [s_lo, s_hi) of its query tiles only
-    const int per = (n_kv + a.n_split - 1) / a.n_split;
-    const int s_lo = (int)blockIdx.y * per, s_hi = min(n_kv, s_lo + per);
-    lo = max(lo, s_lo);
-#pragma unroll
-    for (int t = 0; t < 2; ++t) hi_t[t] = max(lo, min(hi_t[t], s_hi));
-  }
-  const int hi = max(hi_t[0], hi_t[1]);
-  const bool any = hi > lo;
+  if (BIAS) set_ranges(*key_lo_s, *key_hi_s);
 
   if (warp == 8) {
     // ================================================================ TMA producer
     if (lane == 0 && any) {
-      uint8_t* q_s = smem + C::OFF_Q;
-      for (int t = 0; t < 2; ++t) {
-        if (hi_t[t] <= lo) continue;
-        mbar_arrive_expect_tx(&bars.q_full[t], C::TILE);
-        for (int c = 0; c < C::NBOX; ++c)
-          tma_load_3d(q_s + t * C::TILE + c * C::SUB, &a.tm_q, c * (128 / C::EB),
-                      sv.q_off + q_base + t * kBM, sv.hq, &bars.q_full[t]);
-      }
+      if (BIAS) first_loads();
       auto load_k = [&](int j, int stage, uint64_t* bar) {
         for (int c = 0; c < C::NBOX; ++c)
           tma_load_3d(smem + C::OFF_K + stage * C::TILE + c * C::SUB, &a.tm_k, c * (128 / C::EB),
@@ -271,8 +289,6 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
                         sv.k_off + j * kBN, sv.hk, bar);
         }
       };
-      mbar_arrive_expect_tx(bars.k0_full, C::TILE);
-      load_k(lo, 0, bars.k0_full);
       int nkv = 0;   // steps whose loads were issued
       for (int j = lo; j < hi; ++j) {
         const int i = j - lo, s = i % C::NS, u = i / C::NS, s1 = (i + 1) % C::NS;
@@ -342,19 +358,17 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
                    (acc || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = true;
-      for (int t = 0; t < 2 && ok; ++t)
-        if (hi_t[t] > lo) ok = wait_warp(&bars.q_full[t], 0, wc, ERR_WAIT_MMA);
-      if (ok) ok = wait_warp(bars.k0_full, 0, wc, ERR_WAIT_MMA);
-      if (ok) {
+      // S of the first key tile for each query tile as soon as that tile's
+      // Q has landed (the loads go out Q0, K of the first key tile, Q1)
+      bool ok = wait_warp(bars.k0_full, 0, wc, ERR_WAIT_MMA);
+      for (int t = 0; t < 2 && ok; ++t) {
+        if (!active(t, lo)) continue;
+        if (!(ok = wait_warp(&bars.q_full[t], 0, wc, ERR_WAIT_MMA))) break;
         tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (active(t, lo)) {
-            issue_s(t, 0);
-            mma_commit_w(&bars.s_full[t]);
-          }
-        mma_commit_w(bars.k0_empty);
+        issue_s(t, 0);
+        mma_commit_w(&bars.s_full[t]);
       }
+      if (ok) mma_commit_w(bars.k0_empty);
       for (int j = lo; j < hi && ok; ++j) {
         const int i = j - lo, s = i % C::NS, s1 = (i + 1) % C::NS;
         // V_i and K_{i+1}

@@ -37,6 +37,9 @@ DECODE_EXTRA = "bf16_b8h32_q1_k32768_d128_decode"
 METRIC = "attention fwd/bwd TFLOP/s (bf16, causal, d=128) and % of GB300 tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# NVIDIA's nominal dense (no 2:4 sparsity) bf16 tensor rate of one GB300, for
+# context beside the measured peaks
+NOMINAL_BF16_TFLOPS = 2250.0
 
 
 def flops(w):
@@ -191,8 +194,50 @@ def cpu_baseline(w, budget_s=12.0):
             break
         n_rows = max(nh, int(n_rows * min(8.0, budget_s / max(dt, 1e-3))))
         dt, conv, desc, nh = oracle_sample(w, n_rows, seed_offset=1 + i)
-    return {"value": conv / dt / 1e12, "unit": UNIT, "cores": nh, "kind": "oracle",
-            "sample": desc, "seconds": round(dt, 3)}
+    out = {"value": conv / dt / 1e12, "unit": UNIT, "cores": nh, "kind": "oracle",
+           "sample": desc, "seconds": round(dt, 3)}
+    out.update(one_thread_head(w))
+    return out
+
+
+def one_thread_head(w, n_rows=256):
+    """The oracle on ONE thread for `n_rows` evenly spaced query rows of one head
+    (forward rows + their full backward contributions), extrapolated to the whole
+    head by the conventional FLOP count of the sampled vs all rows."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    x = workloads.make_inputs(w.with_(B=1, H=1), seed=w.seed + 778, with_dO=True)
+    f = lambda t: np.ascontiguousarray(t[0, 0].to(torch.float64).numpy())
+    qh, kh, vh, dOh = f(x["q"]), f(x["k"]), f(x["v"]), f(x["dO"])
+    bias = None if x["bias"] is None else np.ascontiguousarray(x["bias"][0].double().numpy())
+    rows = np.unique(np.linspace(0, w.Nq - 1, min(n_rows, w.Nq)).round().astype(np.int64))
+
+    def visible(r):
+        if w.causal:
+            return np.minimum(r + (w.Nk - w.Nq) + 1, w.Nk).clip(min=0).astype(np.float64)
+        return np.full(r.shape, float(w.Nk))
+    t0 = time.perf_counter()
+    oracle.fwd_head_rows(qh, kh, vh, bias, rows, w.scale, w.causal)
+    if w.backward:
+        oracle.bwd_head_rows(qh, kh, vh, bias, dOh, rows, w.scale, w.causal)
+    dt = time.perf_counter() - t0
+    frac = float(visible(rows).sum()) / float(visible(np.arange(w.Nq)).sum())
+    return {"one_thread_head_seconds_extrapolated": round(dt / frac, 3),
+            "one_thread_head_sample": "%d of %d query rows of one head on one thread "
+                                      "(%.3f s), scaled by their share of the head's FLOPs"
+                                      % (len(rows), w.Nq, dt)}
+
+
+def bench_config(w, world):
+    """The `config` object of the JSON line; both arms print the same one."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+            "causal": w.causal, "step": "fa_fwd + fa_bwd",
+            "flop_convention": "fwd 4*B*H*Nq*Nk*d, bwd 2.5x fwd, halved for causal",
+            "l2": "inputs larger than L2 (q,k,v,dO 64 MiB each + outputs), no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 def run_reference(args):
@@ -219,8 +264,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk,
-                       "d": w.d, "causal": w.causal},
+            "config": bench_config(w, args.gpus),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": nh, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -251,6 +295,118 @@ def replica_throughput(ms_total_local, steps, flops_per_step, world, device=None
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     ms_step = float(t.item()) / steps
     return ms_step, flops_per_step * world / (ms_step * 1e-3) / 1e12
+
+def l2_flush_buffer(dev):
+    """A 256 MiB buffer (about twice the 129 MB L2); writing it between timed
+    launches evicts the previous launch's inputs and outputs from L2."""
+    import torch
+    return torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+
+def time_launches(fn, stream, flush, iters=10, warmup=3):
+    """Median milliseconds of fn() over `iters` launches, each bracketed by its
+    own CUDA events on `stream`, with L2 flushed (outside the events) before
+    each one."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    stream.synchronize()
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
+def effective_fwd_flops(w, key_len):
+    """Forward FLOPs over the keys that are not masked: 4*H*Nq*d per valid key
+    (key padding: L_b valid keys in batch b), halved for causal."""
+    valid = float(sum(int(x) for x in key_len)) if key_len is not None else float(w.B * w.Nk)
+    return 4.0 * w.H * w.Nq * valid * w.d * (0.5 if w.causal else 1.0)
+
+
+def measure_configs(fa, dev, stream, rank, headline_parts):
+    """Every workload the hot path is specified on, timed per launch with L2
+    flushed between launches: throughput at the FLOP convention and as a
+    fraction of the measured burst bf16 peak. Inputs are N(0,1) drawn on the
+    device (a seeded device generator); the key-padding lengths are drawn on
+    the host with the recipe of workloads.make_inputs."""
+    import torch
+    peaks, _ = load_peaks()
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    flush = l2_flush_buffer(dev)
+    out = {}
+
+    def rec(ms, fl, eff=None):
+        r = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_of_burst_peak":
+             fl / (ms * 1e-3) / 1e12 / peak}
+        if eff is not None:
+            r["effective_tflops"] = eff / (ms * 1e-3) / 1e12
+        return r
+
+    for name in ("f32_b1h1_n128_d64", "bf16_b4h16_n2048_d64", "bf16_b2h32_n8192_d128_causal",
+                 "bf16_b4h16_n4096_d128_causal_bwd", "bf16_b8h16_q1024_k16384_d128_keypad"):
+        w = workloads.WORKLOADS[name]
+        g = torch.Generator(device=dev).manual_seed(w.seed + 31 * rank)
+        dt = torch.float32 if w.dtype == "fp32" else torch.bfloat16
+        q, dO = (torch.randn((w.B, w.H, w.Nq, w.d), generator=g, device=dev, dtype=dt)
+                 for _ in range(2))
+        k, v = (torch.randn((w.B, w.H, w.Nk, w.d), generator=g, device=dev, dtype=dt)
+                for _ in range(2))
+        bias, key_len = None, None
+        if w.key_padding:
+            gh = torch.Generator().manual_seed(w.seed + 31 * rank)
+            key_len = torch.randint(w.Nk // 2, w.Nk + 1, (w.B,), generator=gh).tolist()
+            bias = torch.zeros((w.B, w.Nk), dtype=torch.float32)
+            for b, L in enumerate(key_len):
+                bias[b, L:] = float("-inf")
+            bias = bias.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+        for causal in ((False, True) if name == "bf16_b4h16_n2048_d64" else (w.causal,)):
+            wc = w.with_(causal=causal)
+            kw = dict(key_bias=bias, causal=causal, scale=w.scale)
+            key = name + ("_causal" if causal and "causal" not in name else "")
+            f_fwd = flops(wc)[0]
+            ms = time_launches(lambda: fa.fwd(q, k, v, out=o, lse=lse, **kw), stream, flush)
+            if w.dtype == "fp32":
+                out[key] = {"fwd": {"us": ms * 1e3}}
+                continue
+            ent = {"fwd": rec(ms, f_fwd, effective_fwd_flops(wc, key_len) if bias is not None
+                              else None)}
+            if name != "bf16_b2h32_n8192_d128_causal":
+                ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d),
+                                 dtype=torch.uint8, device=dev)
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                fa.fwd(q, k, v, out=o, lse=lse, **kw)
+                bk = dict(workspace=ws, dq=dq, dk=dk, dv=dv, **kw)
+                ms_b = time_launches(lambda: fa.bwd(q, k, v, o, lse, dO, **bk), stream, flush)
+                # the main launch alone (after one preprocess; repeating it only
+                # adds more into the dQ accumulator, the work is the same)
+                fa.bwd(q, k, v, o, lse, dO, stage="preprocess", **bk)
+                ms_m = time_launches(lambda: fa.bwd(q, k, v, o, lse, dO, stage="main", **bk),
+                                     stream, flush)
+                eff_b = (2.5 * effective_fwd_flops(wc, key_len) if bias is not None else None)
+                ent["bwd"] = rec(ms_b, 2.5 * f_fwd, eff_b)
+                ent["bwd_main"] = rec(ms_m, 2.5 * f_fwd, eff_b)
+                del ws, dq, dk, dv
+            if name == WORKLOAD:
+                ent["in_step_ms_median"] = {n: statistics.median(v_)
+                                            for n, v_ in headline_parts.items()}
+            out[key] = ent
+        torch.cuda.synchronize(dev)
+        fa.check_device_error(dev)
+        del q, k, v, dO, o, lse, bias
+    del flush
+    out["timing"] = ("per launch, CUDA events on the launching stream, median of 10 after 3 "
+                     "warm-ups, L2 flushed (256 MiB write) before each launch; FLOPs: forward "
+                     "4*B*H*Nq*Nk*d, backward 2.5x, halved for causal; key padding: nominal "
+                     "(all Nk keys) and effective (valid keys only) counts")
+    return out
+
 
 def run_ours(args):
     import torch
@@ -408,24 +564,9 @@ def run_ours(args):
     if not args.no_extras:
         we = workloads.WORKLOADS[FWD_EXTRA]
         g = torch.Generator(device=dev).manual_seed(we.seed + rank)
-        qe, ke, ve = (torch.randn((we.B, we.H, we.Nq, we.d), generator=g, device=dev,
-                                  dtype=torch.bfloat16) for _ in range(3))
-        oe = torch.empty_like(qe)
-        le = torch.empty(qe.shape[:3], dtype=torch.float32, device=dev)
-        for _ in range(3):
-            fa.fwd(qe, ke, ve, out=oe, lse=le, causal=True, scale=we.scale)
+        extras["configs"] = measure_configs(fa, dev, stream, rank, parts)
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n_e = 20
-        b0.record(stream)
-        for _ in range(n_e):
-            fa.fwd(qe, ke, ve, out=oe, lse=le, causal=True, scale=we.scale)
-        b1.record(stream)
-        torch.cuda.synchronize(dev)
-        fa.check_device_error(dev)
-        ms_e = b0.elapsed_time(b1) / n_e
-        extras[FWD_EXTRA + "_fwd_tflops"] = flops(we)[0] / (ms_e * 1e-3) / 1e12
-        extras[FWD_EXTRA + "_fwd_ms"] = ms_e
-        del qe, ke, ve, oe, le
         # decode step through the split-KV forward: HBM-bound (K and V read once)
         wd = workloads.WORKLOADS[DECODE_EXTRA]
         qd, kd, vd = (torch.randn((wd.B, wd.H, n, wd.d), generator=g, device=dev,
@@ -616,23 +757,25 @@ def run_ours(args):
     dom_flops = f_bwd if dom == "bwd_main" else f_fwd
     mean_dom = sum(parts[dom]) / len(parts[dom])
     achieved = dom_flops / (mean_dom * 1e-3) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # The timed region is milliseconds long and runs at the maximum SM clock
+    # (see "clocks"), so the denominator is the burst peak; the sustained one
+    # (a seconds-long loop under the power cap) is reported beside it.
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     traffic = TRAFFIC_BYTES.get(dom)
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                "peak_source": "%s (sustained bf16 dense)" % peak_src,
-                "frac_of_burst_peak": achieved / peaks.get("bf16_tflops", 1900.0)}
+                "peak_source": "%s (burst bf16 dense)" % peak_src,
+                "frac_of_sustained_peak": achieved / sustained,
+                "frac_of_nominal_peak": achieved / NOMINAL_BF16_TFLOPS,
+                "nominal_peak": NOMINAL_BF16_TFLOPS}
     cpu = cpu_baseline(w) if world == 1 else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), bf16)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
-                   "causal": w.causal, "step": "fa_fwd + fa_bwd",
-                   "flop_convention": "fwd 4*B*H*Nq*Nk*d, bwd 2.5x fwd, halved for causal",
-                   "l2": "inputs larger than L2 (q,k,v,dO 64 MiB each + outputs), no flush",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": bench_config(w, world),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,

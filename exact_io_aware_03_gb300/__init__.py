@@ -275,7 +275,9 @@ def _stream(t):
 
 
 def fwd(q, k, v, key_bias=None, causal=False, scale=None, out=None, lse=None):
-    """O [B,H,Nq,d] (q's dtype) and LSE [B,H,Nq] (fp32) for CUDA tensors [B,H,N,d]."""
+    """O [B,H,Nq,d] (q's dtype) and LSE [B,H,Nq] (fp32) for CUDA tensors [B,H,N,d].
+
+    Calls fa_fwd (fa_fwd_gqa when k, v have fewer heads than q)."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, n)
@@ -290,11 +292,18 @@ def fwd(q, k, v, key_bias=None, causal=False, scale=None, out=None, lse=None):
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
-        st = fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(key_bias), _ptr(out), _ptr(lse),
-                        B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)), _dtype_code(q),
+        if Hkv == H:
+            name = "fa_fwd"
+            st = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(key_bias), _ptr(out), _ptr(lse),
+                        B, H, Nq, Nk, d, float(scale), int(bool(causal)), _dtype_code(q),
                         _stream(q))
+        else:
+            name = "fa_fwd_gqa"
+            st = fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(key_bias), _ptr(out), _ptr(lse),
+                            B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                            _dtype_code(q), _stream(q))
     if st != FA_OK:
-        raise FaError(st, "fa_fwd_gqa")
+        raise FaError(st, name)
     return out, lse
 
 
@@ -428,6 +437,8 @@ def bwd(q, k, v, o, lse, dO, key_bias=None, causal=False, scale=None, workspace=
         dq=None, dk=None, dv=None, stage=None, deterministic=False):
     """dQ, dK, dV (q's dtype) for CUDA tensors; o and lse from ``fwd`` on the same inputs.
 
+    Calls fa_bwd (fa_bwd_gqa when k, v have fewer heads than q).
+
     stage: None runs the whole backward (fa_bwd); "preprocess", "main" or
     "postprocess" runs only that launch (the three in order equal fa_bwd).
     deterministic: use fa_bwd_deterministic (bitwise reproducible dq); its
@@ -462,7 +473,10 @@ def bwd(q, k, v, o, lse, dO, key_bias=None, causal=False, scale=None, workspace=
         if st != FA_OK:
             raise FaError(st, fn.__name__)
         return dq, dk, dv
-    if stage is None:
+    if stage is None and Hkv == H:
+        fn = fa_bwd
+        heads = (B, H)
+    elif stage is None:
         fn = fa_bwd_gqa
         heads = (B, H, Hkv)
     else:

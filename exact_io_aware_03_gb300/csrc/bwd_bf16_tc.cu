@@ -185,7 +185,8 @@ struct BwdCfg {
   // the deterministic form stages them in the Q stages (one item per CTA)
   static constexpr bool DK_IN_Q = !DET && 2 * TILE > 32768;
   static constexpr int OFF_SCALARS = OFF_BAR + NBAR * 8;
-  static constexpr int BYTES = OFF_SCALARS + 16 + 2 * 48;   // flags, then the work-item ring
+  static constexpr int BYTES = OFF_SCALARS + 16 + 2 * 64;   // flags, then the work-item ring
+  static_assert(BYTES <= 232448, "shared memory per CTA");
 };
 
 // The kernel's mbarriers: one array in shared memory, each barrier at a fixed
@@ -235,6 +236,7 @@ struct BwdBars {
 // that the last items to start are the short ones.
 struct BwdItem {
   int b, h_q0, grp, key0, Nq, Nk, i0, nqh;
+  int rot;    // the query tiles are walked from i0 + rot, wrapping around
   int n;      // query-tile steps: every query head of the group x query tiles [i0, n_qt)
   long off;   // Nk - Nq: bottom-right causal alignment
   SeqView sv;
@@ -269,6 +271,11 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdBf16Args& a, int w) {
     t.i0 = need <= 0 ? 0 : (int)min((long)n_qt, (need + kT - 1) / kT);
   }
   t.nqh = n_qt - t.i0;
+  // Without a causal mask every key tile of a head walks the same query
+  // tiles; starting each at a different one keeps the items of a head that
+  // run at the same time from reduce-adding into the same dQ rows at once.
+  // (Under a causal mask the items start at their diagonal tiles already.)
+  t.rot = CAUSAL ? 0 : (t.key0 / kT) % max(t.nqh, 1);
   t.n = t.key0 < t.Nk ? max(0, t.nqh) * t.grp : 0;
   return t;
 }
@@ -279,6 +286,7 @@ struct BwdSlot {
   int w;          // item index; -1: no more items
   int n;          // query-tile steps (0: nothing to compute, dK = dV = 0)
   int i0, nqh;    // query tiles [i0, i0 + nqh) of each query head (nqh >= 1)
+  int rot;        // first query tile walked: i0 + rot (then wrapping around)
   int off;        // Nk - Nq of the sequence
   int key0;       // first key of the tile
   int qc0;        // coordinate of the group's first query head in q / dO / dq
@@ -288,6 +296,7 @@ struct BwdSlot {
   int g0;         // global index of the item's first query-tile step
   int kph;        // ordinal of the item among the CTA's items with n > 0
 };
+static_assert(sizeof(BwdSlot) <= 64, "two ring slots fit the 128 bytes after the flags");
 
 // Warp-collective: whether any key of the item's tile has a finite bias (a
 // tile whose keys are all masked out contributes nothing: dK = dV = 0).
@@ -365,7 +374,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
   // the head's coordinate in q/dO/dq
   auto q_head = [&](const BwdItem& t, int lt) { return t.h_q0 + lt / max(t.nqh, 1); };
   auto q_coord = [&](const BwdItem& t, int h) { return p.cu_q ? h : t.b * p.H + h; };
-  auto q_row0 = [&](const BwdItem& t, int lt) { return (t.i0 + lt % max(t.nqh, 1)) * kT; };
+  auto q_row0 = [&](const BwdItem& t, int lt) {
+    const int nqh = max(t.nqh, 1);
+    return (t.i0 + (lt % nqh + t.rot) % nqh) * kT;
+  };
 
   if (warp >= C::W_PROD) {
   if constexpr (!DET) setmaxnreg_dec<C::REG_LO>();
@@ -404,6 +416,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
             sl->n = n;
             sl->i0 = t.i0;
             sl->nqh = max(t.nqh, 1);
+            sl->rot = t.rot;
             sl->off = (int)t.off;
             sl->key0 = t.key0;
             sl->qc0 = p.cu_q ? t.h_q0 : t.b * p.H + t.h_q0;
@@ -660,7 +673,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
         tc_fence_before();
         mbar_arrive_warp(bars.dq_empty());
         const int nqh = cur->nqh;
-        const int row0 = cur->q_off + (cur->i0 + lt % nqh) * kT + qw * 32;
+        const int row0 = cur->q_off + (cur->i0 + (lt % nqh + cur->rot) % nqh) * kT + qw * 32;
         const int qc = cur->qc0 + lt / nqh;
 #pragma unroll
         for (int b2 = 0; b2 < NB; b2 += 2) {
@@ -712,7 +725,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
     // -> 0, kept in fp32 registers for dS; packed bf16 copy to TMEM for dV.
     float P[64];
     auto compute_p = [&](int gi) -> bool {
-      const int q0 = (cur->i0 + (gi - cur->g0) % cur->nqh) * kT;
+      const int q0 = (cur->i0 + ((gi - cur->g0) % cur->nqh + cur->rot) % cur->nqh) * kT;
       const int off = cur->off, key = cur->key0 + r;
       // this tile's base-2 LSE (staged by TMA with Q) for this warpgroup's columns
       if (!wait_warp(&bars.q_full()[gi & 1], (gi >> 1) & 1, wc, ERR_WAIT_SOFTMAX)) return false;

@@ -14,6 +14,35 @@
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
+namespace fa {
+
+// The current device's context id, unique for the life of the process (a
+// context created after cudaDeviceReset gets a new one). The driver entry
+// point is looked up once; the device's primary context is made current
+// first if the runtime has not done so yet.
+fa_status current_context_id(unsigned long long* id) {
+  using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static std::mutex mu;
+  static CtxGetIdFn fn = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!fn) {
+      void* f = nullptr;
+      cudaDriverEntryPointQueryResult q{};
+      const cudaError_t e =
+          cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f) return FA_ERR_CUDA;
+      fn = reinterpret_cast<CtxGetIdFn>(f);
+    }
+  }
+  if (fn(nullptr, id) == CUDA_SUCCESS) return FA_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
+  return fn(nullptr, id) == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace fa
+
 namespace {
 
 __device__ uint32_t g_fa_err_word;
@@ -21,6 +50,7 @@ __device__ uint32_t g_fa_err_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 uint32_t* g_err_ptr[kMaxDevices];
+unsigned long long g_err_ctx[kMaxDevices];   // context id each address belongs to
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -44,12 +74,17 @@ fa_status get_encode(EncodeTiledFn* out) {
 
 fa_status get_err_ptr(uint32_t** out) {
   int dev = 0;
+  unsigned long long ctx = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  if (fa::current_context_id(&ctx) != FA_OK) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_ptr[dev]) {
+  // looked up again when the device's context is not the one the cached
+  // address belongs to (after cudaDeviceReset the module is reloaded)
+  if (!g_err_ptr[dev] || g_err_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_fa_err_word) != cudaSuccess || !p) return FA_ERR_CUDA;
     g_err_ptr[dev] = static_cast<uint32_t*>(p);
+    g_err_ctx[dev] = ctx;
   }
   *out = g_err_ptr[dev];
   return FA_OK;

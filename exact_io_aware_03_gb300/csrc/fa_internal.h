@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa.h"
+
 namespace fa {
 
 // Problem description shared by all kernels. q, o, dO, dq are [B][H][Nq][d];
@@ -113,6 +115,10 @@ struct BwdBf16Args {
   int nq_pad;          // Nq rounded up to a multiple of 128
   int head_group;      // dQ kernel: heads per CTA-ordering group (set by its launcher)
 };
+
+// Id of the current device's context (unique for the life of the process);
+// device-variable addresses cached per device are valid only for this id.
+fa_status current_context_id(unsigned long long* id);
 
 cudaError_t launch_fwd_f32(const FwdF32Args& a, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const FwdBf16Args& a, cudaStream_t s);

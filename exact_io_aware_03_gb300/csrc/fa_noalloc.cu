@@ -24,14 +24,18 @@
 //    does not matter, because the first launch of the backward rewrites every
 //    part of the workspace it later reads (it zeroes the dQ accumulator).
 //  - the first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress, with that device current) and caches it; make
-//    that first call before any stream capture.
+//    (cudaGetSymbolAddress, with that device current) and caches it with the
+//    id of the device's context; make that first call before any stream
+//    capture. After cudaDeviceReset the device gets a new context (and the
+//    array a new address): the next call sees the new id and looks the
+//    address up again, so it too should come before any capture.
 #include <cstdint>
 #include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "fa.h"
+#include "fa_internal.h"
 
 namespace {
 
@@ -40,18 +44,23 @@ static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_S
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices];
+unsigned long long g_scratch_ctx[kMaxDevices];   // context id each address belongs to
 
 // Device address of the scratch array on the current device (looked up once
-// per device; in host code the array's name is only a host-side stand-in).
+// per device and context; in host code the array's name is only a host-side
+// stand-in).
 fa_status scratch_on_current_device(void** out) {
   int dev = 0;
+  unsigned long long ctx = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  if (fa::current_context_id(&ctx) != FA_OK) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_fa_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_addr[dev];
   return FA_OK;

@@ -306,6 +306,10 @@ fa_status fa_bwd_varlen_deterministic(const void *q, const void *k, const void *
  *     be serialised by the caller;
  *   - the first call on a device looks up the array's address on that device
  *     (the current one); make that first call before any stream capture.
+ *     After cudaDeviceReset the device's next context holds the array at a
+ *     new address: the library notices the new context and looks the address
+ *     up again on the next call, which should likewise come before any
+ *     capture.
  */
 fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                          const float *lse, const void *dO,

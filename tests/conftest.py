@@ -10,6 +10,18 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
 
 
+def pytest_sessionfinish(session, exitstatus):
+    """With FA_PARITY_REPORT=<path>, write every parity comparison of the run
+    (achieved max-abs, relative L2, bf16 floor and the gates) to <path>
+    (markdown) and <path>.json."""
+    path = os.environ.get("FA_PARITY_REPORT")
+    if not path:
+        return
+    import parity
+    if parity.REPORT:
+        parity.write_report(path)
+
+
 def read_golden(name):
     """Parse a tests/golden/*.txt fixture: 'key = numbers' lines, '#' comments.
 

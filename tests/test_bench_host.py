@@ -46,3 +46,19 @@ def test_peaks_fall_back_when_the_measured_file_is_absent(tmp_path, monkeypatch)
     peaks, source = bench.load_peaks()
     assert source == "fallback"
     assert peaks == bench.FALLBACK_PEAKS
+
+
+def test_effective_flops_count_only_valid_keys():
+    w = workloads.WORKLOADS["bf16_b8h16_q1024_k16384_d128_keypad"]
+    lens = [w.Nk // 2] * w.B
+    # half of the keys valid in every batch: half of the nominal count
+    assert bench.effective_fwd_flops(w, lens) == 0.5 * bench.flops(w)[0]
+    assert bench.effective_fwd_flops(w, None) == bench.flops(w)[0]
+
+
+def test_both_arms_print_the_same_config():
+    w = workloads.WORKLOADS[bench.WORKLOAD]
+    assert bench.bench_config(w, 1) == bench.bench_config(w, 1)
+    cfg = bench.bench_config(w, 1)
+    assert cfg["workload"] == w.name and cfg["parallelism"] == "single GPU"
+    assert bench.bench_config(w, 4)["parallelism"] == "replicas"

@@ -166,19 +166,22 @@ def test_bwd_full_size_sampled(name):
     dq, dk, dv = run_fwd_bwd(x["q"], x["k"], x["v"], x["dO"], x["bias"], w.causal, w.scale)
     for t in (dq, dk, dv):
         assert bool(torch.isfinite(t.float()).all())
-    heads, rows = workloads.sample_rows(w, 48)
+    # dQ: 192 random rows plus the whole first and last query tiles of 2 heads;
+    # dK, dV: 8 whole heads (the first, the last and 6 seeded others)
+    heads, rows = workloads.sample_rows_dense(w, 192, n_tile_heads=2)
     dq_r = oracle.bwd_dq_rows(x["q"], x["k"], x["v"], x["bias"], x["dO"], heads, rows,
                               scale=w.scale, causal=w.causal)
     H = w.H
     dq_s = torch.stack([dq[h // H, h % H, r] for h, r in zip(heads, rows)])
-    compare("dQ[sampled rows]", dq_s, dq_r, extra=name)
-    whole = [0, w.B * w.H - 1, 5]
+    tag = name + " bwd"
+    compare("dQ[sampled rows]", dq_s, dq_r, extra=tag)
+    whole = workloads.sample_heads(w, 8)
     _, dk_r, dv_r = oracle.bwd_heads(x["q"], x["k"], x["v"], x["bias"], x["dO"], whole,
                                      scale=w.scale, causal=w.causal)
     dk_s = torch.stack([dk[h // H, h % H] for h in whole])
     dv_s = torch.stack([dv[h // H, h % H] for h in whole])
-    compare("dK[sampled heads]", dk_s, dk_r, extra=name)
-    compare("dV[sampled heads]", dv_s, dv_r, extra=name)
+    compare("dK[8 heads]", dk_s, dk_r, extra=tag)
+    compare("dV[8 heads]", dv_s, dv_r, extra=tag)
     if x["bias"] is not None:
         for h in whole:
             dead = torch.isinf(x["bias"][h // H])

@@ -151,12 +151,14 @@ def test_fwd_full_size_sampled_rows(name, causal):
     w = workloads.WORKLOADS[name]
     x = workloads.make_inputs(w, with_dO=False)
     o, lse = run_fwd(x["q"], x["k"], x["v"], x["bias"], causal, w.scale)
-    heads, rows = workloads.sample_rows(w, 96)
+    # 512 random rows plus the whole first and last query tiles of 4 heads
+    heads, rows = workloads.sample_rows_dense(w, 512, n_tile_heads=4)
     o_ref, lse_ref = oracle.fwd_rows(x["q"], x["k"], x["v"], x["bias"], heads, rows,
                                      scale=w.scale, causal=causal)
     H = w.H
     o_s = torch.stack([o[h // H, h % H, r] for h, r in zip(heads, rows)])
     l_s = torch.stack([lse[h // H, h % H, r] for h, r in zip(heads, rows)])
-    compare("O[sampled]", o_s, o_ref, extra=name)
-    compare_lse(l_s, lse_ref, extra=name)
+    tag = name + (" causal" if causal else "") + " fwd"
+    compare("O[sampled]", o_s, o_ref, extra=tag)
+    compare_lse(l_s, lse_ref, extra=tag)
     assert bool(torch.isfinite(o.float()).all())

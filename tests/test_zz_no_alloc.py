@@ -5,9 +5,9 @@ only their buffers, code inside an allocator callback, a service that may not
 call cudaMalloc on its request path) get the backward's workspace from a fixed
 array inside the library instead of from their own allocation. These tests
 call that entry point through the C ABI and check it against fa_bwd, which
-takes a caller-allocated workspace, on two calls in a row (the array is
-shared and keeps the previous call's contents, which must not leak into the
-result). The file is named to be collected last.
+takes a caller-allocated workspace, and against the fp64 oracle, on two calls
+in a row (the array is shared and keeps the previous call's contents, which
+must not leak into the result). The file is named to be collected last.
 """
 import math
 
@@ -16,6 +16,7 @@ import pytest
 import torch
 
 import exact_io_aware_03_gb300 as fa
+import oracle
 from parity import compare
 
 
@@ -72,6 +73,23 @@ def test_noalloc_matches_fa_bwd_on_two_calls(lib, B, H, Nq, Nk, d, causal, pad):
             compare(name, g, r, extra="no-alloc call %d" % call)
         # dK and dV involve no cross-CTA accumulation: identical to fa_bwd's
         assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_the_oracle(lib):
+    """The same entry point checked against the fp64 oracle directly (not only
+    against fa_bwd), on a small causal key-padding case, twice in a row."""
+    B, H, Nq, Nk, d, causal = 1, 2, 300, 300, 64, True
+    q, k, v, dO, bias = _inputs(B, H, Nq, Nk, d, seed=4242, pad=True)
+    scale = d ** -0.5
+    qd, kd, vd, dOd, bd = (t.cuda() for t in (q, k, v, dO, bias))
+    o, lse = fa.fwd(qd, kd, vd, key_bias=bd, causal=causal, scale=scale)
+    ref = oracle.bwd(q, k, v, bias, dO, scale=scale, causal=causal)
+    for call in range(2):
+        got = _noalloc(qd, kd, vd, o, lse, dOd, bd, causal, scale)
+        fa.check_device_error()
+        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+            compare(name, g, r, extra="no-alloc vs oracle, call %d" % call)
 
 
 def test_noalloc_rejects_problems_larger_than_its_array(lib):

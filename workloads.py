@@ -114,6 +114,41 @@ def sample_rows(w: Workload, n: int, seed: int = 7):
     return heads.numpy(), rows.numpy()
 
 
+def sample_rows_dense(w: Workload, n: int, n_tile_heads: int = 4, seed: int = 7, tile: int = 128):
+    """``sample_rows(w, n)`` plus every row of the first and the last
+    ``tile``-row query tile of ``n_tile_heads`` heads (the first, the last and
+    seeded others). The first tile of a causal head holds row 0 (whose output
+    is V_0) and the rows with the fewest keys, where outputs are largest.
+    Returns (heads, rows) as int64 numpy arrays, duplicates removed."""
+    import numpy as np
+    heads, rows = sample_rows(w, n, seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    BH = w.B * w.H
+    picks = [0, BH - 1] + torch.randint(0, BH, (max(0, n_tile_heads - 2),), generator=g).tolist()
+    extra_h, extra_r = [], []
+    for h in dict.fromkeys(picks[:max(1, n_tile_heads)]):
+        for r in list(range(min(tile, w.Nq))) + list(range(max(0, w.Nq - tile), w.Nq)):
+            extra_h.append(h)
+            extra_r.append(r)
+    pairs = np.unique(np.stack([np.concatenate([heads, np.asarray(extra_h, dtype=np.int64)]),
+                                np.concatenate([rows, np.asarray(extra_r, dtype=np.int64)])]),
+                      axis=1)
+    return pairs[0], pairs[1]
+
+
+def sample_heads(w: Workload, n: int, seed: int = 11):
+    """n distinct flat head indices b*H+h: the first, the last and seeded others."""
+    g = torch.Generator().manual_seed(seed)
+    BH = w.B * w.H
+    out = [0, BH - 1]
+    for h in torch.randperm(BH, generator=g).tolist():
+        if len(out) >= min(n, BH):
+            break
+        if h not in out:
+            out.append(h)
+    return out[:min(n, BH)]
+
+
 def varlen_lengths(n: int, seed: int, cap: int = 4096, lo: int = 64):
     """n sequence lengths drawn from a log-normal (median ~1000) clipped to
     [lo, cap] -- the ragged-batch shape used to compare packed and padded

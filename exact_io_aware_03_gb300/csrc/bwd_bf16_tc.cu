@@ -975,11 +975,19 @@ cudaError_t launch_main(const BwdBf16Args& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const long BHkv = (long)a.p.B * a.p.Hkv;
   const long n_items = BHkv * ((a.p.Nk + kT - 1) / kT);
-  // heads per ordering group: the Q and dO every item of a key/value head
-  // streams (all query heads of its group) within ~48 MiB of L2
-  const long q_bytes = 2L * (a.p.H / a.p.Hkv) * a.p.Nq * D * 2;
+  // Heads per ordering group. Every item of a key/value head streams the Q
+  // and dO tiles of its query heads and reduce-adds into their dQ rows, while
+  // each item's K/V tile is read once and passes through L2. A group of
+  // about 1024 items (several waves of CTAs) keeps enough heads in flight
+  // that few items reduce into the same dQ rows at once, and its Q, dO and
+  // fp32 dQ accumulator are kept within 64 MiB so that the streaming K/V
+  // does not evict them.
+  const long n_kt = (a.p.Nk + kT - 1) / kT;
+  const long head_bytes = (long)(a.p.H / a.p.Hkv) * a.p.Nq * D * (2 + 2 + 4);
+  const long g_items = (1024 + n_kt - 1) / n_kt;
+  const long g_l2 = (64L << 20) / std::max(head_bytes, 1L);
   BwdBf16Args b = a;
-  b.head_group = (int)std::max(1L, std::min(BHkv, (48L << 20) / std::max(q_bytes, 1L)));
+  b.head_group = (int)std::max(1L, std::min(BHkv, std::min(g_items, g_l2)));
   long grid = n_items;
   if (!DET) {
     // persistent: one CTA per SM, items from the counter

@@ -57,6 +57,14 @@ def make(B, H, Nq, Nk, d, dtype=torch.bfloat16, seed=0, bias=None):
     elif bias == "all_masked_first_batch":
         b = torch.randn(B, Nk, generator=g)
         b[0] = -math.inf
+    elif bias == "zero_holes":
+        # 0 / -inf, but not a plain padding mask: masked keys inside the
+        # valid range, and a masked prefix in the second batch
+        b = torch.zeros(B, Nk)
+        b[:, 5::9] = -math.inf
+        b[:, Nk - Nk // 3:] = -math.inf
+        if B > 1:
+            b[1, :Nk // 4] = -math.inf
     return q, k, v, b
 
 
@@ -71,6 +79,8 @@ SMALL = [
     (2, 2, 129, 1000, 128, False, "pad"),     # key padding
     (2, 2, 200, 333, 64, True, "finite"),     # finite bias + causal
     (2, 1, 130, 260, 128, False, "all_masked_first_batch"),
+    (2, 2, 200, 700, 128, False, "zero_holes"),
+    (2, 2, 300, 517, 64, True, "zero_holes"),
     (1, 1, 1, 1, 64, False, None),            # degenerate sizes
     (1, 1, 1, 300, 128, True, None),
     (3, 1, 257, 1, 128, False, None),

@@ -50,7 +50,6 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
 constexpr int kBM = 128;       // rows per query tile (= TMEM lanes)
 constexpr int kBN = 128;       // keys per key tile
 constexpr float kLog2e = 1.4426950408889634f;
@@ -73,6 +72,9 @@ struct FwdCfg {
   // O staging: the Q buffers (bf16), or a buffer of its own (FP8 tiles are smaller)
   static constexpr int OFF_OST = FP8 ? OFF_V + NS * TILE : OFF_Q;
   static constexpr int OFF_MISC = FP8 ? OFF_OST + 2 * OTILE : OFF_V + NS * TILE;
+  // warp roles: softmax warps 0-7, then the TMA producer and the MMA issuer
+  static constexpr int W_TMA = 8, W_MMA = 9;
+  static constexpr int NT = 320;
   // misc: bias buffers [2 tiles][2 bufs][128] floats, then barriers
   static constexpr int OFF_BIAS = OFF_MISC;
   static constexpr int OFF_BAR = OFF_BIAS + 2 * 2 * kBN * 4;
@@ -132,6 +134,8 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SCALARS + 4);
   int* key_lo_s = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 8);
   int* key_hi_s = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 12);
+  int* nfin_s = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 16);   // keys with a finite bias
+  int* nzf_s = reinterpret_cast<int*>(smem + C::OFF_SCALARS + 20);    // a finite bias != 0 seen
   float* bias_buf = reinterpret_cast<float*>(smem + C::OFF_BIAS);
   const WaitCtx wc{abort_flag, a.err};
 
@@ -219,7 +223,7 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
   // ---- set-up: barriers, TMEM, optional scan of the bias row. Without a
   // bias the producer thread issues the first loads right after initialising
   // the barriers, under the rest of the set-up.
-  if (warp == 8 && lane == 0) {
+  if (warp == C::W_TMA && lane == 0) {
     mbar_init(&bars.q_full[0], 1);
     mbar_init(&bars.q_full[1], 1);
     for (int s = 0; s < C::NS; ++s) {
@@ -240,28 +244,37 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
     *key_lo_s = Nk;
     if (sv.bad && pair == n_pairs - 1) atomicOr(a.err, ERR_BAD_SEQLEN);
     *key_hi_s = -1;
+    *nfin_s = 0;
+    *nzf_s = 0;
     fence_mbar_init();
     tma_prefetch_desc(&a.tm_q);
     tma_prefetch_desc(&a.tm_k);
     tma_prefetch_desc(&a.tm_v);
     if (!BIAS && any) first_loads();
   }
-  if (warp == 9) {
+  if (warp == C::W_MMA) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   __syncthreads();
   if (BIAS) {
-    // first and last key with a finite bias; tiles outside are skipped
-    int klo = Nk, khi = -1;
-    for (int j = threadIdx.x; j < Nk; j += kThreads) {
-      if (bias_row[j] != -INFINITY) {
+    // first and last key with a finite bias (tiles outside are skipped), how
+    // many keys have one, and whether any of those is not 0
+    int klo = Nk, khi = -1, cnt = 0;
+    bool nz = false;
+    for (int j = threadIdx.x; j < Nk; j += C::NT) {
+      const float bj = bias_row[j];
+      if (bj != -INFINITY) {
         klo = min(klo, j);
         khi = max(khi, j);
+        ++cnt;
+        nz |= (bj != 0.f);
       }
     }
     if (klo < Nk) atomicMin(key_lo_s, klo);
     if (khi >= 0) atomicMax(key_hi_s, khi);
+    if (cnt) atomicAdd(nfin_s, cnt);
+    if (nz) atomicOr(nzf_s, 1);
   }
   tc_fence_before();
   __syncthreads();
@@ -269,8 +282,15 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
   const uint32_t tmem = *tmem_slot;
 
   if (BIAS) set_ranges(*key_lo_s, *key_hi_s);
+  // A bias that is 0 on keys [0, khi] and -inf past them is a key-padding
+  // mask: adding it is the same as hiding the keys past khi, which the
+  // softmax warps then do like the ragged tail of a key range, without the
+  // per-tile bias values.
+  const bool pad_only = BIAS && *nzf_s == 0 && *nfin_s == *key_hi_s + 1;
+  const bool use_bias = BIAS && !pad_only;
+  const long key_last = pad_only ? (long)*key_hi_s : (long)Nk - 1;
 
-  if (warp == 8) {
+  if (warp == C::W_TMA) {
     // ================================================================ TMA producer
     if (lane == 0 && any) {
       if (BIAS) first_loads();
@@ -313,7 +333,7 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
       for (int t = 0; t < 2; ++t)
         if (hi_t[t] > lo) wait1(&bars.q_full[t], 0, wd, ERR_WAIT_DRAIN);
     }
-  } else if (warp == 9) {
+  } else if (warp == C::W_MMA) {
     // ================================================================ MMA issuer
     // (the whole warp, converged; one elected lane issues each instruction)
     if (any) {
@@ -405,16 +425,15 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
     const float sl2 = p.scale * sqk * kLog2e;
     const long off = (long)Nk - Nq;
     // last visible key of this row / of the tile's first row (tile-uniform)
-    const long lim_row = CAUSAL ? min((long)row_g + off, (long)Nk - 1) : (long)Nk - 1;
-    const long lim_tile =
-        CAUSAL ? min((long)(q_base + t * kBM) + off, (long)Nk - 1) : (long)Nk - 1;
+    const long lim_row = CAUSAL ? min((long)row_g + off, key_last) : key_last;
+    const long lim_tile = CAUSAL ? min((long)(q_base + t * kBM) + off, key_last) : key_last;
     float m = -INFINITY, l = 0.f;
     const int n_t = hi_t[t] - lo;
     int i = 0;
     for (; i < n_t; ++i) {
       const int j = lo + i;
       const int key0 = j * kBN;
-      if (BIAS) {
+      if (use_bias) {
         float* bb = bias_buf + (t * 2 + (i & 1)) * kBN;
         const int kj = key0 + r;
         bb[r] = kj < Nk ? bias_row[kj] * kLog2e : -INFINITY;
@@ -430,7 +449,7 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
       tmem_ld_wait();
 
       const bool need_mask = (long)key0 + kBN - 1 > lim_tile;
-      const bool scaled = BIAS || need_mask;
+      const bool scaled = use_bias || need_mask;
       // Scores are handled in pairs with the packed f32x2 instructions, and
       // the row max with the three-input max: about three instructions per
       // score in total.
@@ -440,15 +459,21 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
         const long lim_rel = lim_row - key0;
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
-          const uint64_t b2 = BIAS ? *reinterpret_cast<const uint64_t*>(bb + c) : 0ull;
-          float v0, v1;
-          f2_unpack(fma2(f2_pack(s[c], s[c + 1]), sl2x2, b2), v0, v1);
-          if (need_mask && c > lim_rel) v0 = -INFINITY;
-          if (need_mask && c + 1 > lim_rel) v1 = -INFINITY;
-          s[c] = v0;
-          s[c + 1] = v1;
-          m4[(c / 2) & 3] = fmax3(m4[(c / 2) & 3], v0, v1);
+        for (int c = 0; c < kBN; c += 4) {
+          // four bias values per shared-memory load (the same address in
+          // every lane: a broadcast)
+          float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (use_bias) b4 = *reinterpret_cast<const float4*>(bb + c);
+          float v[4];
+          f2_unpack(fma2(f2_pack(s[c], s[c + 1]), sl2x2, f2_pack(b4.x, b4.y)), v[0], v[1]);
+          f2_unpack(fma2(f2_pack(s[c + 2], s[c + 3]), sl2x2, f2_pack(b4.z, b4.w)), v[2], v[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (need_mask && c + e > lim_rel) v[e] = -INFINITY;
+            s[c + e] = v[e];
+          }
+          m4[(c / 2) & 3] = fmax3(m4[(c / 2) & 3], v[0], v[1]);
+          m4[(c / 2 + 1) & 3] = fmax3(m4[(c / 2 + 1) & 3], v[2], v[3]);
         }
       } else {
 #pragma unroll
@@ -630,7 +655,7 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::W_MMA) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -638,14 +663,14 @@ __device__ __forceinline__ void fwd_body(const FwdBf16Args& a) {
 }
 
 template <int D, bool CAUSAL, bool BIAS>
-__global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdBf16Args a) {
+__global__ void __launch_bounds__(FwdCfg<D, false>::NT, 1) fwd_bf16_kernel(const __grid_constant__ FwdBf16Args a) {
   fwd_body<D, CAUSAL, BIAS, false>(a);
 }
 
 // The same forward on e4m3 operands (kind::f8f6f4 MMAs at twice the bf16
 // rate): S from e4m3 Q, K with per-head scales, P rounded to e4m3 for PV.
 template <int D, bool CAUSAL, bool BIAS>
-__global__ void __launch_bounds__(kThreads, 1) fwd_fp8_kernel(const __grid_constant__ FwdBf16Args a) {
+__global__ void __launch_bounds__(FwdCfg<D, true>::NT, 1) fwd_fp8_kernel(const __grid_constant__ FwdBf16Args a) {
   fwd_body<D, CAUSAL, BIAS, true>(a);
 }
 
@@ -704,7 +729,7 @@ cudaError_t launch_one(const FwdBf16Args& a, cudaStream_t s) {
   FwdBf16Args b = a;
   b.head_group = (int)std::max(1L, std::min(BH, (48L << 20) / std::max(kv_bytes, 1L)));
   const dim3 grid((unsigned)(BH * n_pairs), (unsigned)std::max(1, a.n_split));
-  kern<<<grid, kThreads, C::SMEM_ALLOC, s>>>(b);
+  kern<<<grid, C::NT, C::SMEM_ALLOC, s>>>(b);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_split <= 1) return e;
   const long rows = BH * a.p.Nq;
@@ -742,7 +767,7 @@ cudaError_t launch_fp8_one(const FwdBf16Args& a, cudaStream_t s) {
   FwdBf16Args b = a;
   b.head_group = (int)std::max(1L, std::min(BH, (48L << 20) / std::max(kv_bytes, 1L)));
   b.n_split = 1;
-  kern<<<(unsigned)(BH * n_pairs), kThreads, C::SMEM_ALLOC, s>>>(b);
+  kern<<<(unsigned)(BH * n_pairs), C::NT, C::SMEM_ALLOC, s>>>(b);
   return cudaGetLastError();
 }
 }  // namespace

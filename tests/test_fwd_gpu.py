@@ -134,7 +134,7 @@ def test_fwd_f32_workload_full_parity():
     x = workloads.make_inputs(w)
     o, lse = run_fwd(x["q"], x["k"], x["v"], None, w.causal, w.scale)
     o_ref, lse_ref = oracle.fwd(x["q"], x["k"], x["v"], scale=w.scale)
-    compare("O", o, o_ref, dtype="fp32")
+    compare("O", o, o_ref, dtype="fp32", extra=w.name + " fwd")
     assert float(np.abs(lse.double().numpy() - lse_ref).max()) <= 1e-5
 
 

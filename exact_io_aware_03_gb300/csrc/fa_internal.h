@@ -86,6 +86,11 @@ struct FwdBf16Args {
   const float* amax_q;
   const float* amax_k;
   const float* amax_v;
+  // persistent form: the unit counter (set to 0xFFFFFFFF on the launch's
+  // stream; it lives in the LSE word of the last unit's first row) and the
+  // number of units; nullptr: one unit per CTA
+  uint32_t* sched;
+  int n_units;
 };
 
 // Per-head e4m3 scale: x ~= scale * e4m3(x / scale), scale = max|x| / 448

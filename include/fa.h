@@ -75,6 +75,12 @@ typedef enum {
  * Computes: tiling + online softmax ("FlashAttention, Explained", §13; the
  * query-tile-outer order of §20); causal tile skipping ("Understanding
  * FlashAttention Pt 1", §3.5).
+ * Scheduling: with more query-tile pairs x heads than SMs (bf16, no bias),
+ * one word of lse (row 0 of the last head) serves as the kernel's work
+ * counter while the call runs: it is set with a memset on `stream` before the
+ * kernel and holds that row's LSE when the kernel ends. lse must therefore
+ * not be read or written by other work until the call has completed on
+ * `stream`, as for any output.
  */
 fa_status fa_fwd(const void *q, const void *k, const void *v, const float *key_bias,
                  void *o, float *lse,

@@ -129,6 +129,87 @@ def test_fwd_bf16_increasing_scores_force_every_rescale():
     compare_lse(lse, lse_ref)
 
 
+# More units (query-tile pairs x heads) than the GB300's 152 SMs and no
+# bias: the persistent form, where each CTA claims further units from a
+# counter kept in the LSE word of the last head's first row. Includes a last
+# pair with one inactive query tile (Nq = 384, 640), Nq < Nk and Nq > Nk with
+# ragged key tails, d = 64 and d = 128, causal and not.
+PERSISTENT = [
+    # B, H, Nq, Nk, d, causal
+    (1, 80, 512, 512, 64, False),
+    (1, 77, 384, 384, 128, False),
+    (2, 40, 640, 1000, 128, False),
+    (3, 30, 512, 300, 64, False),
+    (1, 80, 512, 512, 64, True),
+    (2, 40, 640, 1000, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", PERSISTENT)
+def test_fwd_bf16_persistent_full_parity(B, H, Nq, Nk, d, causal):
+    q, k, v, _ = make(B, H, Nq, Nk, d, seed=7 * H + Nq)
+    scale = d ** -0.5
+    o, lse = run_fwd(q, k, v, None, causal, scale)
+    o_ref, lse_ref = oracle.fwd(q, k, v, scale=scale, causal=causal)
+    tag = "(%d,%d,%d,%d,%d,causal=%s)" % (B, H, Nq, Nk, d, causal)
+    compare("O", o, o_ref, extra=tag)
+    compare_lse(lse, lse_ref, extra=tag)
+
+
+def test_fwd_bf16_persistent_counter_row_lse_zero():
+    # The counter's word is the LSE of row 0 of the last head. Make that LSE
+    # exactly 0 (one key, and q . k = 0 on that row): it is stored as -0.
+    B, H, Nq, Nk, d = 1, 160, 256, 1, 64
+    q, k, v, _ = make(B, H, Nq, Nk, d, seed=3)
+    q[0, H - 1, 0] = 0
+    o, lse = run_fwd(q, k, v, None, False, d ** -0.5)
+    o_ref, lse_ref = oracle.fwd(q, k, v, scale=d ** -0.5, causal=False)
+    assert float(lse[0, H - 1, 0]) == 0.0 and lse_ref[0, H - 1, 0] == 0.0
+    compare("O", o, o_ref)
+    compare_lse(lse, lse_ref)
+
+
+def test_fwd_bf16_persistent_counter_row_dead():
+    # causal with Nq > Nk: the last head's first query tile sees no key, so
+    # the counter's word ends as LSE = -inf (and that tile's O as 0)
+    q, k, v, _ = make(2, 80, 384, 200, 64, seed=4)
+    o, lse = run_fwd(q, k, v, None, True, 64 ** -0.5)
+    o_ref, lse_ref = oracle.fwd(q, k, v, scale=64 ** -0.5, causal=True)
+    assert np.isneginf(lse_ref[1, 79, 0]) and np.isneginf(float(lse[1, 79, 0]))
+    assert bool((o[1, 79, :128].float() == 0).all())
+    compare("O", o, o_ref)
+    compare_lse(lse, lse_ref)
+
+
+def test_fwd_bf16_persistent_repeat_and_concurrent_streams():
+    # the unit counter is reset on each launch's own stream and lives in that
+    # launch's LSE: repeated launches and launches on two streams at once give
+    # the same bits
+    B, H, N, d = 2, 96, 512, 128
+    q, k, v, _ = make(B, H, N, N, d, seed=11)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = fa.fwd(qd, kd, vd)
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    o_ref, lse_ref = oracle.fwd(q, k, v, scale=d ** -0.5)
+    compare("O", o1.cpu(), o_ref)
+    compare_lse(l1.cpu(), lse_ref)
+    s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    torch.cuda.synchronize()
+    for _ in range(3):
+        with torch.cuda.stream(s_a):
+            oa, la = fa.fwd(qd, kd, vd)
+        with torch.cuda.stream(s_b):
+            ob, lb = fa.fwd(qd, kd, vd)
+        outs += [(oa, la), (ob, lb)]
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    for o, l in outs:
+        assert torch.equal(o, o1)
+        assert torch.equal(l, l1)
+
+
 def test_fwd_f32_workload_full_parity():
     w = workloads.WORKLOADS["f32_b1h1_n128_d64"]
     x = workloads.make_inputs(w)

@@ -1340,14 +1340,17 @@ int sm_count() {
 // be loaded with the previous unit's last step). Measured against one unit
 // per CTA on a GB300: non-causal B=2 H=32 N=8192 d=128 1.36 -> 1.27 ms,
 // B=4 H=16 N=2048 d=64 100 -> 91 us; causal B=4 H=16 N=4096 d=128
-// 203 -> 200 us, B=4 H=16 N=2048 d=64 61 -> 59 us, B=2 H=32 N=8192 d=128
-// 707 -> 713 us.
+// 203 -> 200 us, B=4 H=16 N=2048 d=64 61 -> 59 us, but B=2 H=32 N=8192
+// d=128 (13.5 units per SM) 707 -> 713 us, hence the causal limit below.
 bool use_persistent(const FwdBf16Args& b, long units, int sms) {
   const Problem& p = b.p;
   const bool steps_everywhere =   // the first query-tile pair sees a key
       p.Nk >= 1 && (!p.causal || (long)std::min(2 * kBM - 1, p.Nq - 1) + p.Nk - p.Nq >= 0);
+  // causal: up to 8 units per SM (the per-unit transition then costs less
+  // than one CTA per unit; at 13.5 per SM it cost 1% more)
+  const bool few = !p.causal || units <= 8L * sms;
   return sms > 0 && units > sms && units - sms < (1L << 22) && b.bias == nullptr &&
-         p.cu_q == nullptr && b.n_split <= 1 && b.lse != nullptr && steps_everywhere;
+         p.cu_q == nullptr && b.n_split <= 1 && b.lse != nullptr && steps_everywhere && few;
 }
 
 template <int D, bool CAUSAL, bool BIAS, bool PERSIST>

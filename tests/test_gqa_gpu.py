@@ -24,6 +24,10 @@ def built():
     (1, 6, 1, 257, 257, 64, False, False),     # multi-query
     (2, 4, 4, 130, 520, 128, True, False),     # H_kv == H through the grouped entry
     (2, 8, 4, 200, 1000, 128, False, True),
+    # more query-tile pairs x heads than the 152 SMs: the persistent forward,
+    # with key/value heads shared by 8 and 10 query heads
+    (2, 80, 10, 512, 512, 64, False, False),
+    (1, 96, 12, 512, 700, 128, True, False),
 ])
 def test_gqa_forward_and_backward(B, H, Hkv, Nq, Nk, d, causal, pad):
     g = torch.Generator().manual_seed(H * 100 + Hkv)

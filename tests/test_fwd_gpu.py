@@ -210,6 +210,32 @@ def test_fwd_bf16_persistent_repeat_and_concurrent_streams():
         assert torch.equal(l, l1)
 
 
+def test_fwd_bf16_persistent_cuda_graph_replay():
+    # the counter reset (a memset on the stream) is captured with the kernel:
+    # every replay claims all units again
+    B, H, N, d = 2, 96, 512, 64
+    q, k, v, _ = make(B, H, N, N, d, seed=13)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty_like(qd)
+    lse = torch.empty(B, H, N, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fa.fwd(qd, kd, vd, out=o, lse=lse)   # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fa.fwd(qd, kd, vd, out=o, lse=lse)
+    o_ref, lse_ref = oracle.fwd(q, k, v, scale=d ** -0.5)
+    for _ in range(3):
+        o.zero_()
+        lse.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        fa.check_device_error()
+        compare("O", o.cpu(), o_ref)
+        compare_lse(lse.cpu(), lse_ref)
+
+
 def test_fwd_f32_workload_full_parity():
     w = workloads.WORKLOADS["f32_b1h1_n128_d64"]
     x = workloads.make_inputs(w)

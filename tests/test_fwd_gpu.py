@@ -142,6 +142,11 @@ PERSISTENT = [
     (3, 30, 512, 300, 64, False),
     (1, 80, 512, 512, 64, True),
     (2, 40, 640, 1000, 128, True),
+    # one query row per head (the pair's second tile inactive), 200 heads
+    (1, 200, 1, 300, 64, False),
+    (2, 100, 1, 257, 128, True),
+    # a single ragged row past the last full tile pair
+    (1, 160, 257, 129, 128, False),
 ]
 
 

@@ -159,6 +159,10 @@ struct BwdCfg {
   static constexpr int TILE = kT * D * 2;     // bf16 [128][D]
   static constexpr int SUB = kT * 128;        // one 64-column box
   static constexpr int ND = DET ? 2 : 1;      // dO stages
+  // reduction form at d = 64: dQ issued before dK, and the next step's Q and
+  // dO prefetched into L2 (measured faster together; each alone, and both
+  // at d = 128, slower)
+  static constexpr bool DQ_FIRST = !DET && D == 64;
   // Threads and roles. Reduction form: warps 0-7 P and dS, 8-11 the dQ
   // read-out (one per TMEM lane quarter), 12 TMA, 13 MMA, 14-15 idle (they
   // complete the last warpgroup for the register split); deterministic
@@ -435,6 +439,15 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
       auto load_step = [&](int lt) -> bool {
         const int gi = g + lt, s = gi & 1, uq = gi >> 1;
         const int q0 = q_row0(t, lt), hq = q_head(t, lt);
+        if (C::DQ_FIRST && lt + 1 < n) {
+          // the next step's Q and dO into L2 (d = 64; at d = 128 the extra
+          // requests measured slower)
+          const int q1 = q_row0(t, lt + 1), h1 = q_coord(t, q_head(t, lt + 1));
+          for (int c = 0; c < D / 64; ++c) {
+            tma_prefetch_l2_3d(&a.tm_q, c * 64, t.sv.q_off + q1, h1);
+            tma_prefetch_l2_3d(&a.tm_do, c * 64, t.sv.q_off + q1, h1);
+          }
+        }
         if (uq > 0 && !wait1(&bars.q_empty()[s], (uq - 1) & 1, wc, ERR_WAIT_LOAD)) return false;
         mbar_arrive_expect_tx(&bars.q_full()[s], C::TILE + 2 * kT * 4);
         for (int c = 0; c < D / 64; ++c)
@@ -620,17 +633,32 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
             mma_commit_w(&bars.q_empty()[s]);
           } else {
             // dK += dS^T Q (A = dS^T: K-major view of the dS boxes), which
-            // frees the Q stage, then dQ = dS K
+            // frees the Q stage, and dQ = dS K. d = 128: dK first, so that
+            // the load of Q(i+2) into the stage starts a product earlier;
+            // d = 64 (with the next step's Q and dO prefetched into L2, so
+            // that their loads land sooner): dQ first, so that its read-out
+            // and the next dP start a product earlier.
+            auto issue_dk = [&]() {
 #pragma unroll
-            for (int kk = 0; kk < kT / 16; ++kk)
-              mma_ss_w(t_dk, sdesc_offset(dk16, C::OFF_DS + (kk / 4) * C::SUB + (kk % 4) * 32),
-                     sdesc_offset(dsub, q_o + kk * 2048), id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
-            mma_commit_w(&bars.q_empty()[s]);
+              for (int kk = 0; kk < kT / 16; ++kk)
+                mma_ss_w(t_dk, sdesc_offset(dk16, C::OFF_DS + (kk / 4) * C::SUB + (kk % 4) * 32),
+                       sdesc_offset(dsub, q_o + kk * 2048), id_acc, (lt > 0 || kk > 0) ? 1u : 0u);
+              mma_commit_w(&bars.q_empty()[s]);
+            };
+            auto issue_dq = [&]() {
 #pragma unroll
-            for (int kk = 0; kk < kT / 16; ++kk)
-              mma_ss_w(t_dp, sdesc_offset(dsub, C::OFF_DS + kk * 2048),
-                     sdesc_offset(dsub, C::OFF_K + kk * 2048), id_dq, kk > 0 ? 1u : 0u);
-            mma_commit_w(bars.dq_full());
+              for (int kk = 0; kk < kT / 16; ++kk)
+                mma_ss_w(t_dp, sdesc_offset(dsub, C::OFF_DS + kk * 2048),
+                       sdesc_offset(dsub, C::OFF_K + kk * 2048), id_dq, kk > 0 ? 1u : 0u);
+              mma_commit_w(bars.dq_full());
+            };
+            if constexpr (C::DQ_FIRST) {
+              issue_dq();
+              issue_dk();
+            } else {
+              issue_dk();
+              issue_dq();
+            }
           }
         }
         // every MMA of this item: its K/V buffers are free, dK and dV final
@@ -868,7 +896,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
           if (lt + 1 < n && !(ok = compute_p(gi + 1))) break;
         }
         if (ok) {
-          // every MMA of the item is done (the last dQ follows the last dK)
+          // every MMA of the item is done (committed after its last product)
           ok = wait_warp(bars.kv_empty(), cur->kph & 1, wc, ERR_WAIT_EPILOGUE);
           tc_fence_after();
         }

@@ -807,12 +807,24 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
       const uint64_t sc2 = f2_pack(p.scale, p.scale);
       if (!wait_warp(bars.dp_full(), gi & 1, wc, ERR_WAIT_SOFTMAX)) return false;
       tc_fence_after();
-      // two chunks of 32 query columns, to keep the live registers low
+      // two chunks of 32 query columns; at d = 128 the second loads while the
+      // first is processed (at d = 64 that measured slower)
+      constexpr bool kPipe = D == 128;
+      uint32_t dpa[64];
+      tmem_ld32(lane_base + 128 + h * 64, dpa);
+      tmem_ld_wait();
+      if (kPipe) tmem_ld32(lane_base + 128 + h * 64 + 32, dpa + 32);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t dpv[32];
-        tmem_ld32(lane_base + 128 + h * 64 + half * 32, dpv);
-        tmem_ld_wait();
+        const uint32_t* dpv = dpa + half * 32;
+        if (half == 1) {
+          if (kPipe) {
+            tmem_ld_wait_regs32(dpa + 32);
+          } else {
+            tmem_ld32(lane_base + 128 + h * 64 + 32, dpa + 32);
+            tmem_ld_wait();
+          }
+        }
         uint32_t dsk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {

@@ -802,7 +802,7 @@ def run_ours(args):
 
 # DRAM bytes per launch of the dominant kernels from an ncu capture, or None
 # when the kernel changed since the counters were taken.
-TRAFFIC_BYTES = {"fwd": 219976960 + 45267968, "bwd_main": 411776256 + 226436352}
+TRAFFIC_BYTES = {"fwd": 219976960 + 45267968, "bwd_main": 411727360 + 226045952}
 
 
 def main():

@@ -679,7 +679,8 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
     // 32 rows, all D columns, out of TMEM at once (the columns go back to the
     // MMA warp for the next dP), then reduce-adds them into the fp32
     // accumulator with TMA in boxes of 32 rows x 32 columns (4 KiB, 128-byte
-    // swizzled), two at a time through its 8 KiB slot of the staging buffer.
+    // swizzled) through its 8 KiB slot of the staging buffer (two boxes per
+    // bulk group at d = 128, one at d = 64).
     const int qw = warp - 8;   // TMEM lane quarter
     const uint32_t lane_base = tmem + ((uint32_t)(qw * 32) << 16);
     uint8_t* slot = smem + C::OFF_DQST + qw * 8192;
@@ -703,26 +704,50 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
         const int nqh = cur->nqh;
         const int row0 = cur->q_off + (cur->i0 + (lt % nqh + cur->rot) % nqh) * kT + qw * 32;
         const int qc = cur->qc0 + lt / nqh;
+        if constexpr (D == 64) {
+          // one bulk group per box; a box waits only for the box two back
+          // (in its half of the slot) to have been read. (At d = 128 this
+          // measured slower than the pairs below.)
 #pragma unroll
-        for (int b2 = 0; b2 < NB; b2 += 2) {
-          if (lane == 0) bulk_wait_group_read0();   // the slot's previous boxes have been read
-          __syncwarp();
-#pragma unroll
-          for (int bb = 0; bb < 2; ++bb) {
+          for (int b = 0; b < NB; ++b) {
+            if (lane == 0) bulk_wait_group_read1();
+            __syncwarp();
+            uint8_t* bx = slot + (b & 1) * 4096;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              const uint32_t* v = x + (b2 + bb) * 32 + 4 * k;
-              *reinterpret_cast<uint4*>(slot + bb * 4096 + lane * 128 + ((k ^ (lane & 7)) * 16)) =
+              const uint32_t* v = x + b * 32 + 4 * k;
+              *reinterpret_cast<uint4*>(bx + lane * 128 + ((k ^ (lane & 7)) * 16)) =
                   make_uint4(v[0], v[1], v[2], v[3]);
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_3d(&a.tm_dqacc, bx, b * 32, row0, qc);
+              bulk_commit_group();
+            }
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
+        } else {
 #pragma unroll
-            for (int bb = 0; bb < 2; ++bb)
-              tma_reduce_add_3d(&a.tm_dqacc, slot + bb * 4096, (b2 + bb) * 32, row0, qc);
-            bulk_commit_group();
+          for (int b2 = 0; b2 < NB; b2 += 2) {
+            if (lane == 0) bulk_wait_group_read0();   // the slot's previous boxes have been read
+            __syncwarp();
+#pragma unroll
+            for (int bb = 0; bb < 2; ++bb) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const uint32_t* v = x + (b2 + bb) * 32 + 4 * k;
+                *reinterpret_cast<uint4*>(slot + bb * 4096 + lane * 128 + ((k ^ (lane & 7)) * 16)) =
+                    make_uint4(v[0], v[1], v[2], v[3]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+              for (int bb = 0; bb < 2; ++bb)
+                tma_reduce_add_3d(&a.tm_dqacc, slot + bb * 4096, (b2 + bb) * 32, row0, qc);
+              bulk_commit_group();
+            }
           }
         }
       }

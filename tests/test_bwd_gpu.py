@@ -167,10 +167,15 @@ def test_bwd_large_magnitude():
         assert rel <= BF16_REL_L2 + float(np.linalg.norm(bnd) / np.linalg.norm(ref)), (name, rel)
 
 
-@pytest.mark.parametrize("name", ["bf16_b4h16_n4096_d128_causal_bwd",
-                                  "bf16_b8h16_q1024_k16384_d128_keypad"])
-def test_bwd_full_size_sampled(name):
+@pytest.mark.parametrize("name,causal", [("bf16_b4h16_n4096_d128_causal_bwd", None),
+                                         ("bf16_b8h16_q1024_k16384_d128_keypad", None),
+                                         ("bf16_b4h16_n2048_d64", False),
+                                         ("bf16_b4h16_n2048_d64", True)])
+def test_bwd_full_size_sampled(name, causal):
     w = workloads.WORKLOADS[name]
+    if causal is not None:   # the d = 64 workload is run both ways
+        w = w.with_(causal=causal)
+        name = name + (" causal" if causal else "")
     x = workloads.make_inputs(w, with_dO=True)
     dq, dk, dv = run_fwd_bwd(x["q"], x["k"], x["v"], x["dO"], x["bias"], w.causal, w.scale)
     for t in (dq, dk, dv):

@@ -317,10 +317,22 @@ int fa_fwd_splitkv_default_splits(int B, int H, int Nq, int Nk, int d) {
     sms = 148;
   const long ctas = (long)B * H * ((Nq + 255) / 256);
   const long n_kv = (Nk + 127) / 128;
-  // enough CTAs for two waves, each split keeping at least 4 key tiles
-  long splits = (2L * sms + ctas - 1) / ctas;
-  splits = std::min(splits, std::max(1L, n_kv / 4));
-  return (int)std::max(1L, std::min(splits, 128L));
+  // One CTA per (head, query-tile pair, split), in waves of one CTA per SM:
+  // the split count whose grid wastes least of its last wave, i.e. the least
+  // waves(s) * (key tiles per split + ~3 tiles of fixed cost per CTA), with
+  // at least 4 key tiles per split and at most 128 splits.
+  const long max_s = std::max(1L, std::min(128L, n_kv / 4));
+  long best = 1;
+  double best_t = 0.0;
+  for (long s = 1; s <= max_s; ++s) {
+    const double waves = (double)((ctas * s + sms - 1) / sms);
+    const double t = waves * (double)((n_kv + s - 1) / s + 3);
+    if (s == 1 || t < best_t) {
+      best = s;
+      best_t = t;
+    }
+  }
+  return (int)best;
 }
 
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, const float* key_bias,

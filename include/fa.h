@@ -152,8 +152,10 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
  * Flash-Decoding). Same arguments, layout and results as fa_fwd_gqa (bf16 only),
  * plus num_splits >= 1 (1 = no split, no workspace use) and a device
  * workspace of fa_fwd_splitkv_workspace_size(...) bytes, 256-byte aligned.
- * fa_fwd_splitkv_default_splits gives a split count that fills the device
- * (uses the current device's SM count; no launch).
+ * fa_fwd_splitkv_default_splits gives a split count for the current device
+ * (its SM count; no launch): the one whose grid, in waves of one CTA per SM,
+ * leaves the least of its last wave idle, with at least 4 key tiles of 128
+ * keys per split and at most 128 splits.
  */
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
 int fa_fwd_splitkv_default_splits(int B, int H, int Nq, int Nk, int d);

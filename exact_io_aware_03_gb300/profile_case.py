@@ -2,10 +2,12 @@
 
     python -m exact_io_aware_03_gb300.profile_case --workload NAME [--pass fwd|bwd|both]
                                                    [--iters N] [--causal 0|1]
-                                                   [--deterministic]
+                                                   [--deterministic] [--fp8]
+                                                   [--splitkv] [--nk N]
 
 Inputs are the seeded synthetic tensors of `workloads.py`. Each iteration runs
-fa_fwd and/or fa_bwd (or fa_bwd_deterministic) once on the current stream; the script synchronises and
+fa_fwd (or fa_fwd_fp8, or fa_fwd_splitkv with its default split count) and/or
+fa_bwd (or fa_bwd_deterministic) once on the current stream; the script synchronises and
 checks the device error word at the end. Nothing is timed or compared: this
 is the small, self-contained command to put under `ncu`.
 """
@@ -36,11 +38,16 @@ def main(argv=None):
                     help="run fa_bwd_deterministic instead of fa_bwd")
     ap.add_argument("--fp8", action="store_true",
                     help="forward: run fa_fwd_fp8 (e4m3) instead of fa_fwd")
+    ap.add_argument("--splitkv", action="store_true",
+                    help="forward: run fa_fwd_splitkv with its default split count")
+    ap.add_argument("--nk", type=int, default=None, help="override the workload's key count")
     args = ap.parse_args(argv)
 
     w = workloads.WORKLOADS[args.workload]
     if args.causal is not None:
         w = w.with_(causal=bool(args.causal))
+    if args.nk is not None:
+        w = w.with_(Nk=args.nk)
     build.build()
     fa.load()
     dev = torch.device("cuda", 0)
@@ -54,9 +61,16 @@ def main(argv=None):
                     if args.deterministic else fa.fa_bwd_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d))
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if args.splitkv:
+        with torch.cuda.device(dev):
+            ns = fa.fa_fwd_splitkv_default_splits(w.B, w.H, w.Nq, w.Nk, w.d)
+        wsk = torch.empty(max(1, fa.fa_fwd_splitkv_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d, ns)),
+                          dtype=torch.uint8, device=dev)
     for _ in range(args.iters):
         if args.which in ("fwd", "both"):
-            if args.fp8:
+            if args.splitkv:
+                fa.fwd_splitkv(q, k, v, num_splits=ns, out=o, lse=lse, workspace=wsk, **kw)
+            elif args.fp8:
                 fa.fwd_fp8(q, k, v, out=o, lse=lse, **kw)
             else:
                 fa.fwd(q, k, v, out=o, lse=lse, **kw)

@@ -141,6 +141,34 @@ def test_splitkv_workspace_and_validation(lib):
         assert st in (fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED), bad
 
 
+def _sm_count():
+    import torch
+    if torch.cuda.is_available():
+        return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return 148   # the library's count when it cannot query a device
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d", [(8, 32, 1, 32768, 128), (1, 32, 1, 8192, 128),
+                                         (2, 16, 1, 65536, 128), (16, 32, 1, 4096, 128),
+                                         (4, 8, 1, 16384, 64), (1, 1, 1, 300, 64),
+                                         (4, 16, 2048, 2048, 64), (1, 2, 700, 100000, 128)])
+def test_splitkv_default_split_count(lib, B, H, Nq, Nk, d):
+    """The default split count: among 1 .. min(128, key tiles / 4) splits, the
+    one with the least waves(s) * (key tiles per split + 3), where a wave is
+    one CTA per SM and a CTA is one (head, query-tile pair, split); the
+    smallest such count on ties."""
+    sms = _sm_count()
+    ctas = B * H * ((Nq + 255) // 256)
+    n_kv = (Nk + 127) // 128
+    max_s = max(1, min(128, n_kv // 4))
+    cost = {s: -(-ctas * s // sms) * (-(-n_kv // s) + 3) for s in range(1, max_s + 1)}
+    best = min(cost.values())
+    want = min(s for s, c in cost.items() if c == best)
+    got = fa.fa_fwd_splitkv_default_splits(B, H, Nq, Nk, d)
+    assert 1 <= got <= max_s
+    assert got == want, (got, want, cost[got], best)
+
+
 @pytest.mark.parametrize("H,H_kv", [(8, 3), (8, 0), (4, 8), (4, -1)])
 def test_gqa_rejects_bad_head_counts(lib, H, H_kv):
     a = dict(q=FAKE, k=FAKE, v=FAKE, key_bias=None, o=FAKE, lse=FAKE, B=1, H=H, H_kv=H_kv, Nq=16,

@@ -205,6 +205,13 @@ __device__ __forceinline__ void fwd_body_one(const FwdBf16Args& a) {
   const int Nq = sv.len_q, Nk = sv.len_k;
   const int q_base = pair * 2 * kBM;
   const float* bias_row = BIAS ? a.bias + (size_t)b * Nk : nullptr;
+  // packed sequences: the grid is sized by the longest one, and a CTA whose
+  // query-tile pair starts past its sequence's end has no rows; it leaves
+  // before any set-up (the sequence's last CTA reports a bad length first)
+  if (p.cu_q != nullptr && q_base >= Nq) {
+    if (sv.bad && pair == n_pairs - 1 && threadIdx.x == 0) atomicOr(a.err, ERR_BAD_SEQLEN);
+    return;
+  }
 
   // ---- key-tile ranges [lo, hi_t) of the two query tiles, from the keys
   // [klo, khi] that can be visible: the whole sequence, or (with a bias) the

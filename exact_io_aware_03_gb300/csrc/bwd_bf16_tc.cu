@@ -397,26 +397,19 @@ __global__ void __launch_bounds__(BwdCfg<D, DET>::NT, 1) bwd_main_kernel(const _
     int pv_row = 0, pv_hk = 0, pv_sk = 0;
     for (int u = 0; ok; ++u) {
       int w;
-      BwdItem t;
       if (DET) {
         w = u == 0 ? (int)blockIdx.x : -1;
-        if (w >= 0) t = bwd_item<CAUSAL>(a, w);
       } else {
-        // packed sequences: key tiles past a sequence's end have no rows of
-        // dK or dV; they are claimed and passed over here, never published
-        for (;;) {
-          w = lane == 0 ? atomicAdd(a.sched, 1) : 0;
-          w = __shfl_sync(0xffffffffu, w, 0);
-          if (w >= n_items) {
-            w = -1;
-            break;
-          }
-          t = bwd_item<CAUSAL>(a, w);
-          if (p.cu_k == nullptr || t.key0 < t.Nk) break;
-        }
+        w = lane == 0 ? atomicAdd(a.sched, 1) : 0;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (w >= n_items) w = -1;
       }
+      BwdItem t;
       int n = 0;
-      if (w >= 0) n = (!BIAS || bwd_item_any_key(a, t)) ? t.n : 0;
+      if (w >= 0) {
+        t = bwd_item<CAUSAL>(a, w);
+        n = (!BIAS || bwd_item_any_key(a, t)) ? t.n : 0;
+      }
       if (lane == 0) {
         // slot u & 1 is free once item u - 2 is done with it
         if (u >= 2 && !wait1(&bars.sched_empty()[u & 1], ((u >> 1) - 1) & 1, wc, ERR_WAIT_LOAD)) ok = false;

@@ -132,23 +132,29 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 
 // ------------------------------------------------------------------ post
 __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ acc,
-                                                       uint16_t* __restrict__ dq, long n4) {
-  // four float4 loads in flight per thread
+                                                       uint16_t* __restrict__ dq, long n8) {
+  // groups of eight values (two float4 loads, one 16-byte store), four
+  // groups (eight loads) in flight per thread
   constexpr int U = 4;
   const long stride = (long)gridDim.x * blockDim.x;
-  for (long i0 = (long)blockIdx.x * blockDim.x + threadIdx.x; i0 < n4; i0 += stride * U) {
-    float4 v[U];
+  const float4* a4 = reinterpret_cast<const float4*>(acc);
+  for (long i0 = (long)blockIdx.x * blockDim.x + threadIdx.x; i0 < n8; i0 += stride * U) {
+    float4 v[U][2];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const long i = i0 + u * stride;
-      if (i < n4) v[u] = reinterpret_cast<const float4*>(acc)[i];
+      if (i < n8) {
+        v[u][0] = a4[2 * i];
+        v[u][1] = a4[2 * i + 1];
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const long i = i0 + u * stride;
-      if (i < n4)
-        reinterpret_cast<uint2*>(dq)[i] =
-            make_uint2(pack_bf16x2(v[u].x, v[u].y), pack_bf16x2(v[u].z, v[u].w));
+      if (i < n8)
+        reinterpret_cast<uint4*>(dq)[i] =
+            make_uint4(pack_bf16x2(v[u][0].x, v[u][0].y), pack_bf16x2(v[u][0].z, v[u][0].w),
+                       pack_bf16x2(v[u][1].x, v[u][1].y), pack_bf16x2(v[u][1].z, v[u][1].w));
     }
   }
 }
@@ -1098,9 +1104,9 @@ cudaError_t launch_d(const BwdBf16Args& a, cudaStream_t s, unsigned stages) {
     if ((e = launch_bwd_dq(a, s)) != cudaSuccess) return e;
   }
   if (stages & BWD_POST) {
-    const long n4 = rows * D / 4;
-    const long blocks = min((n4 + 255) / 256, (long)a.num_sms * 8);
-    bwd_post_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.dq_acc, a.dq, n4);
+    const long n8 = rows * D / 8;
+    const long blocks = min((n8 + 255) / 256, (long)a.num_sms * 8);
+    bwd_post_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.dq_acc, a.dq, n8);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return e;

@@ -1,5 +1,6 @@
 """Host-side pieces of bench.py, on the CPU: the FLOP convention, the clock
-sampler's parsing of nvidia-smi lines, and the fallback peaks."""
+sampler's parsing of nvidia-smi lines, the fallback peaks, and the reference
+arm's JSON line."""
 import bench
 import workloads
 
@@ -62,3 +63,29 @@ def test_both_arms_print_the_same_config():
     cfg = bench.bench_config(w, 1)
     assert cfg["workload"] == w.name and cfg["parallelism"] == "single GPU"
     assert bench.bench_config(w, 4)["parallelism"] == "replicas"
+
+
+def test_reference_arm_line_carries_the_contract_keys(monkeypatch, capsys):
+    """The reference arm's JSON line (the oracle timed on the host cores):
+    same metric, unit and config as the GPU arm, impl "reference", a
+    cpu_baseline describing the run, and an e2e object with no copies. The
+    oracle's timing is stubbed so that the test runs in no time."""
+    import json
+    import types
+    monkeypatch.setattr(bench, "calibrated_oracle", lambda w, per_step: 8)
+    monkeypatch.setattr(bench, "oracle_sample",
+                        lambda w, n, seed_offset=0: (0.5, 2.0e9, "stub sample", 3))
+    args = types.SimpleNamespace(steps=2, warmup=1, gpus=1)
+    assert bench.run_reference(args) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    w = workloads.WORKLOADS[bench.WORKLOAD]
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["config"] == bench.bench_config(w, 1)
+    assert line["value"] == 2.0e9 / 0.5 / 1e12
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["higher_is_better"] is True
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 3 and cb["value"] == line["value"]
+    assert cb["sample"] == "stub sample"
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
